@@ -1,0 +1,427 @@
+#!/usr/bin/env python
+"""Benchmark of the embedding step on GB300: forward (probe + gather + pool)
+and backward (dedupe + segmented reduce + Adagrad) over one CSR batch of a
+seeded synthetic workload, through the C ABI.
+
+Default workload: the large configuration (64 slots, 100M keys, dim 128,
+float16 weights + float32 accumulators, batch 131,072, Zipf(1.1) bag lengths
+in [1, 256], Zipf(1.1) ids, 5% absent keys, mean pooling).  Its inputs are far
+larger than the 129 MB L2, so no flush is needed between steps.
+
+Prints ONE JSON line (rank 0).  --impl reference times the CPU oracle instead.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+NOMINAL_HBM_GBS = 8000.0
+FALLBACK_HBM_GBS = 6800.0
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--config", type=int, default=5, help="workload 1..5")
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--cpu-samples", type=int, default=2048,
+                    help="samples of the batch the CPU-baseline oracle runs (bounded sample)")
+    ap.add_argument("--ref-samples", type=int, default=128, help="samples per reference-arm step")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
+    return ap.parse_args()
+
+
+def peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(p) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured (MEASURED_PEAKS.json hbm_gbs)"
+    except Exception:
+        return FALLBACK_HBM_GBS, "fallback 6.8 TB/s"
+
+
+class Clocks:
+    """nvidia-smi sampling of SM clocks and throttle reasons during the timed region."""
+
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.f = tempfile.NamedTemporaryFile("w+", suffix=".csv", delete=False)
+        self.p = None
+
+    def start(self):
+        try:
+            self.p = subprocess.Popen(["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.Q}",
+                                       "--format=csv,noheader,nounits", "-lms", "200"],
+                                      stdout=self.f, stderr=subprocess.DEVNULL)
+        except Exception:
+            self.p = None
+
+    def stop(self):
+        if self.p is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.p.terminate()
+        try:
+            self.p.wait(timeout=5)
+        except Exception:
+            self.p.kill()
+        self.f.flush()
+        self.f.seek(0)
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in self.f.read().splitlines():
+            parts = [x.strip() for x in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                mx.append(float(parts[2]))
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[5:9]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        os.unlink(self.f.name)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(mx) if mx else None,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+def dist_init(args):
+    import torch
+    import torch.distributed as dist
+
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if ws > 1 and not dist.is_initialized():
+        dist.init_process_group("nccl" if torch.cuda.is_available() else "gloo")
+    return ws, rank, local
+
+
+def barrier(ws):
+    if ws > 1:
+        import torch.distributed as dist
+
+        dist.barrier()
+
+
+def max_over_ranks(ws, x: float) -> float:
+    if ws == 1:
+        return x
+    import torch
+    import torch.distributed as dist
+
+    t = torch.tensor([x], dtype=torch.float64, device="cuda" if torch.cuda.is_available() else "cpu")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def launches_per_step(n_keys: int) -> int:
+    """Kernels this library launches for one fwd + one bwd call."""
+    bits = max(1, int(n_keys).bit_length())
+    passes = max(1, math.ceil(bits / 8))
+    return 1 + 1 + passes * 5 + 2   # fwd; expand; (count + 3 scan + scatter) per radix pass; reduce; fixup
+
+
+# ------------------------------------------------------------------ oracle (CPU baseline / reference arm)
+
+class OracleRunner:
+    """The CPU oracle on bounded samples (prefixes of whole samples) of the batch."""
+
+    def __init__(self, cfg, keys_np, off_np, q_np, grad_np):
+        import numpy as np
+
+        import oracle
+
+        self.np = np
+        self.oracle = oracle
+        self.cfg = cfg
+        t0 = time.time()
+        self.T = oracle.Table(keys_np, cfg.capacity, cfg.dims)
+        self.build_s = time.time() - t0
+        self.keys = keys_np
+        self.off, self.q, self.grad = off_np, q_np, grad_np
+        self.eoff = self.T.elem_offsets() if not cfg.uniform_dim else None
+
+    def prepare(self, b0: int, b1: int):
+        """Inputs for samples [b0, b1): a CSR sub-batch and the initial rows it touches."""
+        import torch
+
+        import workload as W
+
+        np, cfg = self.np, self.cfg
+        S = cfg.n_slots
+        o = self.off[b0 * S:b1 * S + 1]
+        q = self.q[o[0]:o[-1]]
+        off = o - o[0]
+        grad = self.grad[b0:b1]
+        _, rows = self.T.resolve(q)
+        rows = np.unique(rows[rows >= 0])
+        dims_rows = np.array(cfg.dims, dtype=np.int64)[self.keys[rows] >> 48]
+        if cfg.uniform_dim:
+            eoff = torch.arange(0, (self.keys.size + 1) * cfg.dims[0], cfg.dims[0], dtype=torch.int64)
+        else:
+            eoff = torch.from_numpy(self.eoff)
+        vals = W.w0_rows(cfg, eoff, torch.from_numpy(rows), torch.from_numpy(dims_rows)).numpy()
+        row_map = np.full(self.keys.size, -1, dtype=np.int64)
+        starts = np.concatenate([[0], np.cumsum(dims_rows)[:-1]]).astype(np.int64)
+        row_map[rows] = starts
+        return off, q, grad, vals, row_map
+
+    def step(self, prep):
+        """One oracle step on the sample: forward, per-key gradients, Adagrad. Returns seconds."""
+        np, cfg, oracle = self.np, self.cfg, self.oracle
+        off, q, grad, vals, row_map = prep
+        t0 = time.perf_counter()
+        self.T.forward(off, q, cfg.pool, cfg.wdtype, vals, row_map=row_map)
+        uk, rows, goff, G, _ = self.T.backward(off, q, cfg.pool, grad)
+        idx = np.concatenate([np.arange(row_map[r], row_map[r] + (goff[i + 1] - goff[i]))
+                              for i, r in enumerate(rows)]) if rows.size else np.zeros(0, np.int64)
+        oracle.adagrad(G, vals[idx], np.full(idx.size, cfg.acc0, np.float32), cfg.lr, cfg.eps)
+        return time.perf_counter() - t0
+
+
+def host_arrays(wl):
+    return (wl.keys.cpu().numpy(), wl.offsets.cpu().numpy(), wl.qkeys.cpu().numpy(), wl.grad.cpu().numpy())
+
+
+def run_reference(args):
+    """--impl reference: the CPU oracle, timed on the host cores, on samples of the same workload."""
+    import torch
+
+    import workload as W
+
+    ws, rank, local = dist_init(args)
+    if rank != 0:
+        return
+    cfg = W.config(args.config)
+    dev = "cuda" if torch.cuda.is_available() else "cpu"
+    if dev == "cuda":
+        torch.cuda.set_device(local)
+    keys = W.table_keys(cfg, dev).cpu().numpy()
+    off_t, q_t = W.batch(cfg, dev)
+    grad = W.grad_out(cfg, dev).cpu().numpy()
+    runner = OracleRunner(cfg, keys, off_t.cpu().numpy(), q_t.cpu().numpy(), grad)
+    b = max(1, min(args.ref_samples, cfg.batch))
+    times, lookups = [], []
+    for k in range(args.warmup + args.steps):
+        b0 = (k * b) % max(1, cfg.batch - b + 1)
+        prep = runner.prepare(b0, b0 + b)
+        t = runner.step(prep)
+        if k >= args.warmup:
+            times.append(t)
+            lookups.append(prep[1].size)
+    total_t = sum(times)
+    v = sum(lookups) / total_t
+    line = {"metric": "embedding lookups/s (fwd+bwd step)", "value": v, "unit": "lookups/s", "impl": "reference",
+            "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": 1e3 * total_t / len(times), "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": cfg.name, "sample_samples_per_step": b},
+            "cpu_baseline": {"value": v, "unit": "lookups/s", "cores": 1, "kind": "oracle",
+                             "sample": f"{b} samples x {cfg.n_slots} slots per step, rotating through the batch; "
+                                       f"single-threaded oracle, {os.cpu_count()} cores available; "
+                                       f"table build {runner.build_s:.1f}s untimed"},
+            "e2e": {"value": v, "unit": "lookups/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+# ------------------------------------------------------------------ our arm
+
+def run_ours(args):
+    import numpy as np
+    import torch
+
+    import workload as W
+    import sparse_ctr_embedding_gb300 as E
+
+    ws, rank, local = dist_init(args)
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    E.build() if rank == 0 else None
+    barrier(ws)
+    E.build()
+    cfg = W.config(args.config)
+    stream = torch.cuda.current_stream()
+
+    # ---- workload (generated on the device, keys copied to the host for the table build)
+    t0 = time.time()
+    keys = W.table_keys(cfg, dev)
+    offsets, qkeys = W.batch(cfg, dev)
+    grad = W.grad_out(cfg, dev)
+    n_elems = int(sum(cfg.vocab[s] * cfg.dims[s] for s in range(cfg.n_slots)))
+    values = W.w0_values(cfg, n_elems, dev)
+    keys_h = keys.cpu()
+    torch.cuda.synchronize()
+    t_gen = time.time() - t0
+    t0 = time.time()
+    tbl = E.emb_table_create(cfg.dims, cfg.wdtype, keys_h, values=values, capacity=cfg.capacity,
+                             acc_init=cfg.acc0)
+    t_create = time.time() - t0
+    del values
+    torch.cuda.empty_cache()
+    st = tbl.stats
+    nnz = qkeys.numel()
+    n_bags = offsets.numel() - 1
+    out = torch.empty((cfg.batch, cfg.sum_dims), dtype=torch.float32, device=dev)
+    wsb = torch.empty(E.emb_bwd_workspace_size(tbl, n_bags, nnz), dtype=torch.uint8, device=dev)
+
+    # ---- algorithmic bytes of one step (the bytes the method must move)
+    wsz = 2 if cfg.wdtype == "f16" else 4
+    _, rows = E.emb_resolve(tbl, qkeys)
+    hit = rows >= 0
+    dims_t = torch.tensor(cfg.dims, dtype=torch.int64, device=dev)
+    d_occ = dims_t[qkeys >> 48]
+    n_hits = int(hit.sum())
+    gather_bytes = int((d_occ * hit).sum()) * wsz
+    del rows, hit, d_occ
+    p_bar = st["sum_probe"] / max(1, st["n_keys"])
+    io_bytes = 8 * nnz + 16 * nnz * p_bar + 4 * cfg.batch * cfg.sum_dims + 8 * (n_bags + 1)
+    fwd_bytes = io_bytes + gather_bytes
+
+    def step():
+        E.emb_lookup_fwd(tbl, offsets, qkeys, cfg.pool, out=out)
+        E.emb_bwd_adagrad(tbl, offsets, qkeys, cfg.pool, grad, cfg.lr, cfg.eps, wsb)
+
+    step()
+    uk = torch.empty(nnz, dtype=torch.int64, device=dev)
+    nu = torch.zeros(1, dtype=torch.int64, device=dev)
+    E.emb_bwd_unique_keys(tbl, wsb, uk, nu)
+    n_unique = int(nu.item())
+    d_u = dims_t[uk[:n_unique] >> 48]
+    rmw_bytes = int(d_u.sum()) * (2 * wsz + 8)
+    del uk, d_u
+    bwd_bytes = io_bytes + rmw_bytes
+    flags = E.emb_check_device_flag(tbl)
+
+    for _ in range(max(0, args.warmup - 1)):
+        step()
+    torch.cuda.synchronize()
+    barrier(ws)
+    clocks = Clocks(local)
+    clocks.start()
+    K = args.steps
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(K)]
+    for k in range(K):
+        ev[k][0].record(stream)
+        E.emb_lookup_fwd(tbl, offsets, qkeys, cfg.pool, out=out)
+        ev[k][1].record(stream)
+        E.emb_bwd_adagrad(tbl, offsets, qkeys, cfg.pool, grad, cfg.lr, cfg.eps, wsb)
+        ev[k][2].record(stream)
+    torch.cuda.synchronize()
+    barrier(ws)
+    clk = clocks.stop()
+    total_ms = ev[0][0].elapsed_time(ev[K - 1][2])
+    fwd_ms = statistics.mean(e[0].elapsed_time(e[1]) for e in ev)
+    bwd_ms = statistics.mean(e[1].elapsed_time(e[2]) for e in ev)
+    total_ms = max_over_ranks(ws, total_ms)
+    ms_step = total_ms / K
+    flags |= E.emb_check_device_flag(tbl)
+
+    # ---- end to end through the C ABI: pinned host inputs in, pooled output back, every step
+    e2e = None
+    if not args.no_e2e:
+        off_h = offsets.cpu().pin_memory()
+        q_h = qkeys.cpu().pin_memory()
+        g_h = grad.cpu().pin_memory()
+        out_h = torch.empty(out.shape, dtype=out.dtype).pin_memory()
+        h2d = off_h.numel() * 8 + q_h.numel() * 8 + g_h.numel() * 4
+        d2h = out_h.numel() * 4
+
+        def e2e_step():
+            offsets.copy_(off_h, non_blocking=True)
+            qkeys.copy_(q_h, non_blocking=True)
+            grad.copy_(g_h, non_blocking=True)
+            step()
+            out_h.copy_(out, non_blocking=True)
+
+        for _ in range(2):
+            e2e_step()
+        torch.cuda.synchronize()
+        barrier(ws)
+        Ke = max(3, K // 2)
+        a = torch.cuda.Event(enable_timing=True)
+        b = torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        for _ in range(Ke):
+            e2e_step()
+        b.record(stream)
+        torch.cuda.synchronize()
+        e2e_ms = max_over_ranks(ws, a.elapsed_time(b)) / Ke
+        e2e = {"value": ws * nnz / (e2e_ms * 1e-3), "unit": "lookups/s", "ms_per_step": e2e_ms,
+               "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+               "path": "pinned host CSR batch + grad_out -> H2D -> emb_lookup_fwd + emb_bwd_adagrad -> D2H pooled output"}
+
+    peak, peak_src = peaks()
+    fwd_gbs = fwd_bytes / (fwd_ms * 1e-3) / 1e9
+    bwd_gbs = bwd_bytes / (bwd_ms * 1e-3) / 1e9
+    dominant_fwd = fwd_ms >= bwd_ms
+    roof = {"bound": "hbm", "kernel": "fwd_pool_kernel" if dominant_fwd else "bwd (all kernels)",
+            "achieved": fwd_gbs if dominant_fwd else bwd_gbs, "peak": peak, "unit": "GB/s",
+            "frac": (fwd_gbs if dominant_fwd else bwd_gbs) / peak, "traffic": None, "peak_source": peak_src,
+            "algorithmic_bytes_per_launch": fwd_bytes if dominant_fwd else bwd_bytes}
+
+    cpu = None
+    if rank == 0 and ws == 1 and not args.no_cpu_baseline:
+        keys_np, off_np, q_np, g_np = keys_h.numpy(), offsets.cpu().numpy(), qkeys.cpu().numpy(), grad.cpu().numpy()
+        runner = OracleRunner(cfg, keys_np, off_np, q_np, g_np)
+        b = max(1, min(args.cpu_samples, cfg.batch))
+        prep = runner.prepare(0, b)
+        t = runner.step(prep)
+        cpu = {"value": prep[1].size / t, "unit": "lookups/s", "cores": 1, "kind": "oracle",
+               "sample": f"first {b} of {cfg.batch} samples ({prep[1].size} lookups, all {cfg.n_slots} slots): "
+                         f"forward + per-key gradients + Adagrad in {t:.1f}s on 1 of {os.cpu_count()} host cores; "
+                         f"oracle table build {runner.build_s:.1f}s untimed"}
+
+    line = {
+        "metric": "embedding lookups/s (fwd+bwd step)", "value": ws * nnz / (ms_step * 1e-3), "unit": "lookups/s",
+        "n_gpus": ws, "steps": K, "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+        "config": {"workload": cfg.name, "keys": cfg.n_keys, "slots": cfg.n_slots, "dim": cfg.dims[0]
+                   if cfg.uniform_dim else list(cfg.dims), "weights": cfg.wdtype, "batch": cfg.batch,
+                   "bags": n_bags, "nnz": nnz, "hits": n_hits, "unique_keys": n_unique, "pool": cfg.pool,
+                   "l2": "inputs larger than L2 (no flush)", "parallelism": "replicas" if ws > 1 else "single"},
+        "samples_per_s": ws * cfg.batch / (ms_step * 1e-3),
+        "fwd_ms": fwd_ms, "bwd_ms": bwd_ms, "fwd_lookups_per_s": nnz / (fwd_ms * 1e-3),
+        "fwd_algorithmic_gbs": fwd_gbs, "bwd_algorithmic_gbs": bwd_gbs,
+        "fwd_frac_nominal_8tbs": fwd_gbs / NOMINAL_HBM_GBS, "bwd_frac_nominal_8tbs": bwd_gbs / NOMINAL_HBM_GBS,
+        "roofline": roof,
+        "roofline_bwd": {"bound": "hbm", "achieved": bwd_gbs, "peak": peak, "unit": "GB/s", "frac": bwd_gbs / peak,
+                         "algorithmic_bytes_per_step": bwd_bytes},
+        "cpu_baseline": cpu, "e2e": e2e,
+        "gpu_launches": K * launches_per_step(st["n_keys"]),
+        "clocks": clk, "device_flags": flags,
+        "setup_s": {"generate": t_gen, "table_create": t_create},
+    }
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    tbl.close()
+
+
+def main():
+    args = parse()
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_ours(args)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,234 @@
+/*
+ * emb_gb300.h -- C ABI of the GB300 (sm_103a) embedding step over a unified,
+ * insert-free GPU hash table.
+ *
+ * The step, as the pages describe it:
+ *  - Tencent PCG DataFun talk (GPU recommendation-training framework),
+ *    paragraph "各阶段优化详细介绍": before a PASS is trained, every embedding
+ *    vector (and optimizer state) it needs is flashed whole into an embedding
+ *    table in GPU memory; that table is a GPU hashtable whose insert
+ *    operation is removed, because the table structure is prepared
+ *    beforehand and copied to global memory as one block.
+ *  - same talk, paragraph "计算优化" (Unified Hash Table): all features share
+ *    one huge table; keys are int64 with the real key in the low 48 bits and
+ *    the table (slot) id in the high 16 bits; one lookup kernel serves all
+ *    features and one backward kernel updates them; pooling of identical
+ *    parameters is merged ("kernel merge"); FP16 storage allows vectorised
+ *    access and half2 arithmetic.
+ *  - JD ads sparse-training article, section 4.2.1: an EmbeddingBag over a
+ *    flat id list with per-sample offsets, pooled by sum or mean; section
+ *    3.2.1: Adagrad keeps a per-parameter sum of squared gradients, updates
+ *    element-wise, and leaves features absent from the batch untouched.
+ * The hash (MurmurHash3 fmix64), linear probing over a power-of-two table and
+ * the update  acc += g*g; w -= lr*g/(sqrt(acc)+eps)  complete the method.
+ *
+ * Conventions shared by every entry point:
+ *  - Pointers named *_h are host memory; *_d are device memory of the GPU
+ *    that is current when the call is made.  Arguments documented as "host
+ *    or device" accept either (unified addressing).
+ *  - `stream` is a cudaStream_t passed as void*; NULL means the legacy
+ *    default stream.  Calls that take a stream only enqueue work and return;
+ *    kernel-side problems are reported later by emb_check_device_flag().
+ *  - Every call returns an emb_status and never aborts the process; on
+ *    failure emb_last_error() gives a human-readable reason (thread-local).
+ *  - The table owns all of its device memory (slots, weights, accumulators);
+ *    the caller owns every input, output and workspace buffer.
+ *  - Keys: key = (slot << 48) | raw, 0 <= slot < n_slots <= 65535.  The
+ *    all-ones int64 (-1) is the empty-slot sentinel and is never a key.
+ *  - A CSR batch over B samples and S slots has n_bags = B*S bags in
+ *    sample-major order (bag = b*S + s), offsets int64[n_bags+1] with
+ *    offsets[0] = 0, nondecreasing, offsets[n_bags] = nnz, and keys
+ *    int64[nnz].  Bag (b, s) pools only table keys whose slot field is s;
+ *    keys absent from the table (misses) pool as zero vectors.
+ *  - Pooled output and its gradient are float32 [B, sum(dims)], slot s
+ *    occupying columns [col_s, col_s + dim_s) with col_s = sum_{s'<s} dim_s'.
+ */
+#ifndef EMB_GB300_H
+#define EMB_GB300_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#if defined(__GNUC__)
+#define EMB_API __attribute__((visibility("default")))
+#else
+#define EMB_API
+#endif
+
+typedef struct emb_table emb_table; /* opaque; owns the table's device memory */
+
+typedef enum {
+  EMB_OK = 0,
+  EMB_ERR_INVALID_ARG = 1,  /* null pointer, bad size, bad enum, bad layout */
+  EMB_ERR_CUDA = 2,         /* a CUDA runtime call failed */
+  EMB_ERR_OOM = 3,          /* device or host allocation failed */
+  EMB_ERR_DUP_KEY = 4,      /* a key appears twice in emb_table_create */
+  EMB_ERR_RESERVED_KEY = 5, /* the empty sentinel (-1) given as a key */
+  EMB_ERR_LOAD_FACTOR = 6,  /* capacity not a power of two >= 2 * n_keys */
+  EMB_ERR_WORKSPACE = 7,    /* workspace missing or smaller than required */
+  EMB_ERR_DEVICE_FLAG = 8,  /* a kernel reported bad input (see flag bits) */
+  EMB_ERR_UNSUPPORTED = 9   /* a size beyond this library's stated limits */
+} emb_status;
+
+typedef enum { EMB_F32 = 0, EMB_F16 = 1 } emb_dtype; /* weight storage; accumulator is always f32 */
+typedef enum { EMB_POOL_SUM = 0, EMB_POOL_MEAN = 1 } emb_pool;
+
+/* Device flag bits reported by emb_check_device_flag. */
+#define EMB_FLAG_PROBE_BOUND 1u   /* a probe ran past the table's longest cluster (corrupt table) */
+#define EMB_FLAG_BAD_OFFSETS 2u   /* CSR offsets out of [0, nnz] or decreasing; clamped */
+#define EMB_FLAG_SLOT_MISMATCH 4u /* a bag held a key of another slot; it was skipped */
+
+/* Limits of this implementation (EMB_ERR_UNSUPPORTED beyond them). */
+#define EMB_MAX_DIM 512            /* per-slot dim; f32 dims multiple of 4, f16 of 8 */
+#define EMB_MAX_KEYS 2147483647LL  /* rows are indexed with 32 bits */
+#define EMB_MAX_NNZ 2147483647LL   /* per call */
+#define EMB_MAX_BAGS 2147483647LL  /* per call */
+
+typedef struct {
+  int32_t n_slots;         /* feature tables merged into the unified table, 1..65535 */
+  const int32_t* slot_dim; /* host [n_slots]: embedding dim of each slot */
+  emb_dtype wdtype;        /* weight storage type */
+  int64_t capacity;        /* slots: power of two >= 2*n_keys; 0 = the smallest such */
+  float acc_init;          /* accumulator value used when emb_table_create gets acc == NULL */
+} emb_table_desc;
+
+typedef struct {
+  int64_t n_keys;
+  int64_t capacity;
+  int64_t n_elems;     /* weight elements = sum over keys of dim(slot(key)) */
+  int32_t n_slots;
+  int32_t sum_dims;    /* columns of the pooled output */
+  int32_t max_dim;
+  int32_t wdtype;
+  int64_t max_probe;   /* longest probe sequence (slots inspected) of an inserted key */
+  int64_t sum_probe;   /* sum over inserted keys of their probe lengths */
+  int64_t max_cluster; /* longest run of occupied slots */
+  int64_t probe_bound; /* max_cluster + 1: kernels never inspect more slots per key */
+  double load_factor;  /* n_keys / capacity */
+  uint64_t device_bytes;
+} emb_table_stats;
+
+/*
+ * emb_table_create -- prepare the insert-free table and flash it to the GPU
+ * (Tencent PCG talk, "各阶段优化详细介绍"; key layout from "计算优化").
+ *   desc     host: slot count, per-slot dims, weight type, capacity, acc_init.
+ *   keys_h   host int64[n_keys]: the deduplicated keys of the pass, in
+ *            "keys-array order".  Slots are assigned by inserting the keys one
+ *            by one in this order with linear probing from fmix64(key) mod
+ *            capacity, so the layout is a pure function of this array.
+ *   values   host or device, ragged rows in keys-array order: key i's row has
+ *            dim(slot(key_i)) elements of wdtype (float or IEEE half).  NULL
+ *            fills the weights with zeros.
+ *   acc      host or device float32, same element layout as values; NULL fills
+ *            with desc->acc_init.
+ *   stream   stream for the uploads; the call synchronises it before return.
+ *   out      receives the table handle (NULL on failure).
+ * Errors: INVALID_ARG (bad desc, slot field >= n_slots, dims out of range),
+ * RESERVED_KEY, DUP_KEY, LOAD_FACTOR, UNSUPPORTED (n_keys > EMB_MAX_KEYS),
+ * OOM, CUDA.  Nothing is left allocated on failure.
+ */
+EMB_API emb_status emb_table_create(const emb_table_desc* desc, const int64_t* keys_h, int64_t n_keys,
+                            const void* values, const float* acc, void* stream, emb_table** out);
+
+/* Free the table and its device memory.  Work queued on it must be complete. */
+EMB_API emb_status emb_table_destroy(emb_table* table);
+
+/* Host-side statistics of the table (no GPU access). */
+EMB_API emb_status emb_table_get_stats(const emb_table* table, emb_table_stats* out);
+
+/*
+ * emb_table_plan -- validate desc and keys and compute the statistics the
+ * table would have, on the host only (no CUDA call).  Same errors as
+ * emb_table_create apart from OOM/CUDA.  slot_key_h / slot_row_h, if not
+ * NULL, receive the host-built layout: int64[capacity] key per slot (-1 =
+ * empty) and the keys-array index stored there (-1 = empty).
+ */
+EMB_API emb_status emb_table_plan(const emb_table_desc* desc, const int64_t* keys_h, int64_t n_keys,
+                          emb_table_stats* out, int64_t* slot_key_h, int64_t* slot_row_h);
+
+/*
+ * emb_lookup_fwd -- the unified lookup kernel plus merged pooling (Tencent
+ * PCG talk, "计算优化"; JD article 4.2.1): for every bag, probe each key,
+ * gather the rows of the hits and sum them in float32; mean divides by the
+ * bag length L counting misses (L = 0 gives zeros).
+ *   offsets_d  int64[n_bags+1] CSR offsets; n_bags must be a multiple of n_slots.
+ *   keys_d     int64[nnz].
+ *   out_d      float32[n_bags/n_slots, sum_dims], fully overwritten.
+ * Errors (host, before any work): INVALID_ARG, UNSUPPORTED.  Offsets outside
+ * [0, nnz] are clamped and raise EMB_FLAG_BAD_OFFSETS; a key of another slot
+ * is skipped and raises EMB_FLAG_SLOT_MISMATCH.
+ */
+EMB_API emb_status emb_lookup_fwd(emb_table* table, const int64_t* offsets_d, int64_t n_bags, const int64_t* keys_d,
+                          int64_t nnz, emb_pool pool, float* out_d, void* stream);
+
+/* Bytes of device workspace emb_bwd_adagrad needs for this batch shape. */
+EMB_API emb_status emb_bwd_workspace_size(const emb_table* table, int64_t n_bags, int64_t nnz, size_t* bytes);
+
+/*
+ * emb_bwd_adagrad -- the unified backward kernel (Tencent PCG talk, "计算优化")
+ * with element-wise sparse Adagrad (JD article 3.2.1): every hit occurrence of
+ * key k in bag (b, s) contributes grad_out[b, cols of s] (times 1/L for mean)
+ * to G[k]; the contributions of duplicate keys are reduced deterministically
+ * (stable sort by row, fixed-order segmented sums); then for each hit key and
+ * each element:  acc += g*g;  w -= lr*g / (sqrt(acc) + eps)  in float32
+ * (half weights rounded to nearest-even).  Rows not hit are not touched.
+ *   grad_out_d   float32[n_bags/n_slots, sum_dims].
+ *   workspace_d  device scratch of at least emb_bwd_workspace_size() bytes,
+ *                256-byte aligned; after the call it holds the unique rows of
+ *                this step (read them with emb_bwd_unique_keys).
+ * Same input checks as emb_lookup_fwd, plus WORKSPACE.  Two calls that share
+ * a workspace or a table must be ordered on the GPU (same stream or events).
+ */
+EMB_API emb_status emb_bwd_adagrad(emb_table* table, const int64_t* offsets_d, int64_t n_bags, const int64_t* keys_d,
+                           int64_t nnz, emb_pool pool, const float* grad_out_d, float lr, float eps,
+                           void* workspace_d, size_t ws_bytes, void* stream);
+
+/*
+ * emb_bwd_unique_keys -- the deduplicated key set of the last emb_bwd_adagrad
+ * that used this workspace.  keys_out_d int64[>= nnz of that call] receives
+ * the unique hit keys (slot-major internal row order); n_unique_d int64[1]
+ * receives their count.
+ */
+EMB_API emb_status emb_bwd_unique_keys(const emb_table* table, const void* workspace_d, size_t ws_bytes,
+                               int64_t* keys_out_d, int64_t* n_unique_d, void* stream);
+
+/*
+ * emb_resolve -- the probe alone (parity of slot resolution): for each key,
+ * slot_out_d[i] = its slot index in the table or -1, row_out_d[i] = its index
+ * in the keys array given to emb_table_create or -1.  Either output may be NULL.
+ */
+EMB_API emb_status emb_resolve(const emb_table* table, const int64_t* keys_d, int64_t n, int64_t* slot_out_d,
+                       int64_t* row_out_d, void* stream);
+
+/*
+ * emb_table_export -- checkpoint: copy keys, weights and accumulators back in
+ * keys-array order (same layouts as emb_table_create's inputs).  Destinations
+ * are host or device; any may be NULL.  Synchronises `stream`.  Creating a
+ * table from the exported arrays resumes it exactly.
+ */
+EMB_API emb_status emb_table_export(const emb_table* table, int64_t* keys_out, void* values_out, float* acc_out,
+                            void* stream);
+
+/* Copy the slot layout (key and keys-array index per slot, -1 = empty) to
+ * host or device int64[capacity] buffers; either may be NULL.  Synchronises. */
+EMB_API emb_status emb_table_slots(const emb_table* table, int64_t* slot_key_out, int64_t* slot_row_out, void* stream);
+
+/*
+ * emb_check_device_flag -- synchronise `stream`, read and clear the table's
+ * device flag word.  Returns EMB_ERR_DEVICE_FLAG if any EMB_FLAG_* bit was set
+ * by a kernel since the last check (flags_out, if not NULL, receives them).
+ */
+EMB_API emb_status emb_check_device_flag(emb_table* table, void* stream, uint32_t* flags_out);
+
+EMB_API const char* emb_status_string(emb_status s);
+EMB_API const char* emb_last_error(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* EMB_GB300_H */

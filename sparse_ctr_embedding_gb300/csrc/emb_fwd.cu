@@ -1,0 +1,214 @@
+// Forward: unified lookup + merged pooling (kernel F).
+//
+// Tencent PCG DataFun talk, "计算优化": one lookup kernel serves every feature
+// of the unified table, pooling of all slots is merged into it ("kernel
+// merge"), and FP16 rows are read with vector loads.  JD ads article, 4.2.1:
+// per-sample bags pooled by sum or mean.
+//
+// Mapping (one launch for every slot and dim): one warp per bag, grid-stride
+// over bags in CSR order.  The warp resolves up to 32 keys of the bag at once
+// (one key per lane: the probes of 32 keys are in flight together), then its
+// lanes split into P = 32/G groups of G lanes; group p pools keys p, p+P, ...
+// of the chunk, each lane owning 16-byte column vectors of the row.  U keys
+// per group are gathered before any is added, so every lane keeps U x NCB
+// 16-byte loads in flight.  The P partial sums are combined with xor
+// shuffles and group 0 writes the pooled row with 16-byte stores.
+// Accumulation is float32 in a fixed order, so results are deterministic.
+#include "emb_internal.cuh"
+
+namespace emb {
+
+template <typename TW>
+struct VecOf;
+template <>
+struct VecOf<float> {
+  static constexpr int kElems = 4;
+  __device__ __forceinline__ static void add(float* acc, const uint4& v) {
+    acc[0] += __uint_as_float(v.x);
+    acc[1] += __uint_as_float(v.y);
+    acc[2] += __uint_as_float(v.z);
+    acc[3] += __uint_as_float(v.w);
+  }
+};
+template <>
+struct VecOf<__half> {
+  static constexpr int kElems = 8;
+  __device__ __forceinline__ static void add(float* acc, const uint4& v) {
+    const unsigned w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      __half2 h = *reinterpret_cast<const __half2*>(&w[i]);
+      float2 f = __half22float2(h);
+      acc[2 * i] += f.x;
+      acc[2 * i + 1] += f.y;
+    }
+  }
+};
+
+__device__ __forceinline__ uint4 ldg16(const void* p) {
+  uint4 v;
+  asm("ld.global.nc.v4.u32 {%0,%1,%2,%3}, [%4];" : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "l"(p));
+  return v;
+}
+
+__device__ __forceinline__ void st16_streaming(float* p, float a, float b, float c, float d) {
+  asm volatile("st.global.cs.v4.f32 [%0], {%1,%2,%3,%4};" ::"l"(p), "f"(a), "f"(b), "f"(c), "f"(d) : "memory");
+}
+
+__device__ __forceinline__ int pow2_at_least(int x) {
+  int g = 1;
+  while (g < x) g <<= 1;
+  return g;
+}
+
+template <typename TW, int NCB, int U>
+__global__ void __launch_bounds__(256) fwd_pool_kernel(TableView t, const long long* __restrict__ offsets,
+                                                       long long n_bags, const long long* __restrict__ keys,
+                                                       long long nnz, int mean, float* __restrict__ out) {
+  constexpr int VEC = VecOf<TW>::kElems;
+  const int lane = threadIdx.x & 31;
+  const long long nwarps = ((long long)gridDim.x * blockDim.x) >> 5;
+  const TW* W = static_cast<const TW*>(t.W);
+  for (long long bag = (blockIdx.x * (long long)blockDim.x + threadIdx.x) >> 5; bag < n_bags; bag += nwarps) {
+    const int s = (int)((unsigned)bag % (unsigned)t.n_slots);
+    const long long b = (unsigned)bag / (unsigned)t.n_slots;
+    int D, col;
+    long long ebase = 0;
+    unsigned rbase = 0;
+    if (t.uniform_dim) {
+      D = t.uniform_dim;
+      col = s * D;
+    } else {
+      const SlotInfo si = t.sinfo[s];
+      D = si.dim;
+      col = si.col;
+      ebase = si.elem_base;
+      rbase = si.row_base;
+    }
+    const int G = min(32, pow2_at_least(D / VEC));  // lanes per key
+    const int P = 32 / G;                           // keys pooled side by side
+    const int sub = lane / G, li = lane % G;
+
+    long long start = offsets[bag], end = offsets[bag + 1];
+    if (start < 0 || end > nnz || end < start || (bag == 0 && start != 0) || (bag == n_bags - 1 && end != nnz)) {
+      if (lane == 0) atomicOr(t.flags, EMB_FLAG_BAD_OFFSETS);
+      start = min(max(start, 0LL), nnz);
+      end = min(max(end, start), nnz);
+    }
+    float acc[NCB][VEC];
+#pragma unroll
+    for (int c = 0; c < NCB; ++c)
+#pragma unroll
+      for (int j = 0; j < VEC; ++j) acc[c][j] = 0.f;
+
+    for (long long c0 = start; c0 < end; c0 += 32) {
+      const int n = (int)min(32LL, end - c0);
+      long long elem = -1;  // first weight element of this lane's key, -1 = miss
+      if (lane < n) {
+        const long long k = keys[c0 + lane];
+        if (key_slot(k) != s) {
+          atomicOr(t.flags, EMB_FLAG_SLOT_MISMATCH);
+        } else {
+          unsigned row, ext;
+          unsigned long long h;
+          if (probe(t, k, &row, &ext, &h))
+            elem = t.uniform_dim ? (long long)row * D : ebase + (long long)(row - rbase) * D;
+        }
+      }
+      for (int base = 0; base < n; base += P * U) {
+        uint4 v[U][NCB];
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+          const int i = base + u * P + sub;
+          const long long e = __shfl_sync(0xffffffffu, elem, i & 31);
+          const bool ok = (i < n) && (e >= 0);
+#pragma unroll
+          for (int c = 0; c < NCB; ++c) {
+            const int ce = (c * G + li) * VEC;
+            v[u][c] = (ok && ce < D) ? ldg16(W + e + ce) : make_uint4(0u, 0u, 0u, 0u);
+          }
+        }
+#pragma unroll
+        for (int u = 0; u < U; ++u)
+#pragma unroll
+          for (int c = 0; c < NCB; ++c) VecOf<TW>::add(acc[c], v[u][c]);
+      }
+    }
+    // combine the P key groups (fixed xor tree: deterministic)
+#pragma unroll
+    for (int c = 0; c < NCB; ++c)
+#pragma unroll
+      for (int j = 0; j < VEC; ++j)
+        for (int off = G; off < 32; off <<= 1) acc[c][j] += __shfl_xor_sync(0xffffffffu, acc[c][j], off);
+
+    if (sub == 0) {
+      const long long L = end - start;
+      const float den = (mean && L > 0) ? (float)L : 1.f;  // mean over L counting misses; L = 0 gives 0
+      float* o = out + b * t.sum_dims + col;
+#pragma unroll
+      for (int c = 0; c < NCB; ++c) {
+        const int ce = (c * G + li) * VEC;
+        if (ce < D) {
+#pragma unroll
+          for (int j = 0; j < VEC; j += 4)
+            st16_streaming(o + ce + j, acc[c][j] / den, acc[c][j + 1] / den, acc[c][j + 2] / den,
+                           acc[c][j + 3] / den);
+        }
+      }
+    }
+  }
+}
+
+template <typename TW>
+static cudaError_t launch_fwd(const emb_table* t, const long long* offsets, long long n_bags, const long long* keys,
+                              long long nnz, int mean, float* out, cudaStream_t st) {
+  constexpr int VEC = VecOf<TW>::kElems;
+  const int max_vecs = t->st.max_dim / VEC;      // 16-byte vectors in the widest row
+  const int ncb = (max_vecs + 31) / 32;          // column blocks per lane at G = 32
+  const int threads = 256;
+  long long blocks = (n_bags * 32 + threads - 1) / threads;
+  const long long resident = (long long)sm_count() * (2048 / threads);
+  if (blocks > resident) blocks = resident;
+  if (blocks < 1) blocks = 1;
+  TableView v = t->view();
+  if (ncb <= 1)
+    fwd_pool_kernel<TW, 1, 4><<<(int)blocks, threads, 0, st>>>(v, offsets, n_bags, keys, nnz, mean, out);
+  else if (ncb <= 2)
+    fwd_pool_kernel<TW, 2, 2><<<(int)blocks, threads, 0, st>>>(v, offsets, n_bags, keys, nnz, mean, out);
+  else
+    fwd_pool_kernel<TW, 4, 1><<<(int)blocks, threads, 0, st>>>(v, offsets, n_bags, keys, nnz, mean, out);
+  return cudaGetLastError();
+}
+
+emb_status check_batch(const emb_table* t, const int64_t* offsets_d, int64_t n_bags, const int64_t* keys_d,
+                       int64_t nnz, int pool) {
+  if (!t) return fail(EMB_ERR_INVALID_ARG, "table is NULL");
+  if (n_bags < 0 || nnz < 0) return fail(EMB_ERR_INVALID_ARG, "negative n_bags or nnz");
+  if (n_bags > EMB_MAX_BAGS || nnz > EMB_MAX_NNZ) return fail(EMB_ERR_UNSUPPORTED, "batch exceeds EMB_MAX_* limits");
+  if (n_bags % t->st.n_slots != 0) return fail(EMB_ERR_INVALID_ARG, "n_bags must be a multiple of n_slots");
+  if (!offsets_d || (nnz > 0 && !keys_d)) return fail(EMB_ERR_INVALID_ARG, "offsets or keys is NULL");
+  if (pool != EMB_POOL_SUM && pool != EMB_POOL_MEAN) return fail(EMB_ERR_INVALID_ARG, "bad pool mode");
+  return EMB_OK;
+}
+
+}  // namespace emb
+
+using namespace emb;
+
+extern "C" emb_status emb_lookup_fwd(emb_table* table, const int64_t* offsets_d, int64_t n_bags,
+                                     const int64_t* keys_d, int64_t nnz, emb_pool pool, float* out_d,
+                                     void* stream) {
+  emb_status rc = check_batch(table, offsets_d, n_bags, keys_d, nnz, pool);
+  if (rc != EMB_OK) return rc;
+  if (n_bags == 0) return EMB_OK;
+  if (!out_d) return fail(EMB_ERR_INVALID_ARG, "out is NULL");
+  cudaStream_t st = (cudaStream_t)stream;
+  cudaError_t e =
+      table->st.wdtype == EMB_F16
+          ? launch_fwd<__half>(table, (const long long*)offsets_d, n_bags, (const long long*)keys_d, nnz,
+                               pool == EMB_POOL_MEAN, out_d, st)
+          : launch_fwd<float>(table, (const long long*)offsets_d, n_bags, (const long long*)keys_d, nnz,
+                              pool == EMB_POOL_MEAN, out_d, st);
+  if (e != cudaSuccess) return cuda_fail(e, "fwd_pool_kernel launch");
+  return EMB_OK;
+}

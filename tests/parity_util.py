@@ -1,0 +1,133 @@
+"""Helpers for GPU-vs-oracle parity tests (test code only).
+
+Tolerance gates (derived from the arithmetic; tol = 1e-5 for float32 weight
+storage, 2e-3 for float16 storage):
+  pooled output   |x - r| <= tol * max(|r|, A)   A = sum |terms| / (L if mean)
+  accumulator     |x - r| <= tol * r             (r >= acc0 > 0)
+  weight          |x - r| <= tol * max(|r|, |w_old|)
+Index work (slots, rows, unique keys) and untouched rows are compared bit-exactly.
+"""
+from __future__ import annotations
+
+import dataclasses
+from typing import Optional
+
+import numpy as np
+import torch
+
+import oracle
+import workload as W
+import sparse_ctr_embedding_gb300 as E
+
+TOL = {"f32": 1e-5, "f16": 2e-3}
+
+
+def tol_of(cfg) -> float:
+    return TOL[cfg.wdtype]
+
+
+def gate(name, x, r, scale, tol):
+    x = np.asarray(x, dtype=np.float64)
+    r = np.asarray(r, dtype=np.float64)
+    scale = np.asarray(scale, dtype=np.float64)
+    err = np.abs(x - r)
+    bad = err > tol * scale
+    rel = float((err / np.maximum(scale, 1e-300)).max()) if err.size else 0.0
+    if bad.any():
+        i = int(np.argmax(bad))
+        raise AssertionError(f"{name}: {int(bad.sum())}/{bad.size} outside tol {tol}; first at {i}: "
+                             f"x={x.flat[i]!r} r={r.flat[i]!r} scale={scale.flat[i]!r}; max rel {rel:.3g}")
+    return rel
+
+
+@dataclasses.dataclass
+class GpuStep:
+    table: E.Table
+    out: torch.Tensor
+    slots: torch.Tensor
+    rows: torch.Tensor
+    unique: np.ndarray
+    keys_out: np.ndarray
+    values_out: np.ndarray
+    acc_out: np.ndarray
+    flags: int
+    ws: torch.Tensor
+
+
+def make_table(cfg, wl, values_dev=True):
+    vals = wl.values.cuda() if values_dev else wl.values.cpu()
+    return E.emb_table_create(cfg.dims, cfg.wdtype, wl.keys.cpu(), values=vals, acc=None,
+                              capacity=cfg.capacity, acc_init=cfg.acc0)
+
+
+def gpu_step(cfg, wl, values_dev=True) -> GpuStep:
+    tbl = make_table(cfg, wl, values_dev)
+    off, q, g = wl.offsets.cuda(), wl.qkeys.cuda(), wl.grad.cuda()
+    out = E.emb_lookup_fwd(tbl, off, q, cfg.pool)
+    slots, rows = E.emb_resolve(tbl, q)
+    n_bags, nnz = off.numel() - 1, q.numel()
+    ws = torch.empty(E.emb_bwd_workspace_size(tbl, n_bags, nnz), dtype=torch.uint8, device="cuda")
+    E.emb_bwd_adagrad(tbl, off, q, cfg.pool, g, cfg.lr, cfg.eps, ws)
+    uk = torch.empty(max(nnz, 1), dtype=torch.int64, device="cuda")
+    nu = torch.zeros(1, dtype=torch.int64, device="cuda")
+    E.emb_bwd_unique_keys(tbl, ws, uk, nu)
+    n_el = tbl.stats["n_elems"]
+    ko = torch.empty(cfg.n_keys, dtype=torch.int64, device="cuda")
+    vo = torch.empty(n_el, dtype=wl.values.dtype, device="cuda")
+    ao = torch.empty(n_el, dtype=torch.float32, device="cuda")
+    E.emb_table_export(tbl, ko, vo, ao)
+    flags = E.emb_check_device_flag(tbl)
+    torch.cuda.synchronize()
+    return GpuStep(tbl, out, slots, rows, uk[:int(nu.item())].cpu().numpy(), ko.cpu().numpy(),
+                   vo.cpu().numpy(), ao.cpu().numpy(), flags, ws)
+
+
+def elem_index(elem_off: np.ndarray, rows: np.ndarray) -> np.ndarray:
+    starts = elem_off[rows]
+    lens = elem_off[rows + 1] - starts
+    rep = np.repeat(starts, lens)
+    within = np.arange(int(lens.sum())) - np.repeat(np.cumsum(lens) - lens, lens)
+    return rep + within
+
+
+def check_step(cfg, wl, gs: GpuStep, T: Optional[oracle.Table] = None) -> dict:
+    """Full element-wise parity of one step against the oracle."""
+    tol = tol_of(cfg)
+    keys = wl.keys.cpu().numpy()
+    off = wl.offsets.cpu().numpy()
+    q = wl.qkeys.cpu().numpy()
+    values = wl.values.cpu().numpy()
+    grad = wl.grad.cpu().numpy()
+    if T is None:
+        T = oracle.Table(keys, cfg.capacity, cfg.dims)
+    rep = {}
+    assert gs.flags == 0, f"device flag {gs.flags}"
+    # slot resolution and hit mask: bit-exact
+    slot_r, row_r = T.resolve(q)
+    assert np.array_equal(gs.slots.cpu().numpy(), slot_r)
+    assert np.array_equal(gs.rows.cpu().numpy(), row_r)
+    # pooled output
+    out_r, A = T.forward(off, q, cfg.pool, cfg.wdtype, values)
+    rep["fwd_max_rel"] = gate("pooled", gs.out.cpu().numpy(), out_r, np.maximum(np.abs(out_r), A), tol)
+    # unique keys: bit-exact as a set
+    uk_r, rows_u, goff, G, Ag = T.backward(off, q, cfg.pool, grad)
+    assert np.array_equal(np.sort(gs.unique), uk_r)
+    rep["n_unique"] = int(uk_r.size)
+    # checkpoint keys come back in keys-array order
+    assert np.array_equal(gs.keys_out, keys)
+    # updated rows
+    eoff = T.elem_offsets()
+    idx = elem_index(eoff, rows_u)
+    acc0 = np.full(idx.size, cfg.acc0, dtype=np.float32)
+    w_r, acc_r = oracle.adagrad(G, values[idx], acc0, cfg.lr, cfg.eps)
+    rep["acc_max_rel"] = gate("acc", gs.acc_out[idx], acc_r, acc_r, tol)
+    w_old = values[idx].astype(np.float64)
+    rep["w_max_rel"] = gate("weight", gs.values_out[idx].astype(np.float64), w_r.astype(np.float64),
+                            np.maximum(np.abs(w_r.astype(np.float64)), np.abs(w_old)), tol)
+    # rows not hit: bit-identical weights and accumulators
+    untouched = np.ones(values.size, dtype=bool)
+    untouched[idx] = False
+    assert np.array_equal(gs.values_out[untouched].view(np.int16 if values.dtype == np.float16 else np.int32),
+                          values[untouched].view(np.int16 if values.dtype == np.float16 else np.int32))
+    assert np.all(gs.acc_out[untouched] == np.float32(cfg.acc0))
+    return rep

@@ -1,0 +1,76 @@
+"""The C-ABI library without a GPU: symbols, host-side table preparation and
+input validation (emb_table_plan makes no CUDA call)."""
+import ctypes
+
+import numpy as np
+import pytest
+
+import oracle
+import workload as W
+import sparse_ctr_embedding_gb300 as E
+
+
+@pytest.fixture(scope="module", autouse=True)
+def built():
+    E.build()
+
+
+def test_library_exports_every_declared_symbol():
+    declared = E.declared_symbols()
+    assert len(declared) >= 14
+    L = E.lib()
+    for name in declared:
+        assert hasattr(L, name), name
+        assert ctypes.cast(getattr(L, name), ctypes.c_void_p).value
+    assert E.emb_status_string(0) == "ok"
+
+
+@pytest.mark.parametrize("cfg", [W.config(1), W.scaled(W.config(2), 100, 1), W.scaled(W.config(4), 200, 1),
+                                 W.scaled(W.config(5), 1000, 1)], ids=lambda c: c.name)
+def test_host_layout_matches_oracle_bit_exact(cfg):
+    keys = W.table_keys(cfg).numpy()
+    st, sk, sr = E.emb_table_plan(cfg.dims, cfg.wdtype, keys, cfg.capacity, layout=True)
+    T = oracle.Table(keys, cfg.capacity, cfg.dims)
+    ok_, or_ = T.layout()
+    assert np.array_equal(sk, ok_)
+    assert np.array_equal(sr, or_)
+    assert st["max_probe"] == T.max_probe
+    assert st["sum_probe"] == T.sum_probe
+    assert st["max_cluster"] == T.max_cluster
+    assert st["probe_bound"] == T.max_cluster + 1
+    assert st["n_elems"] == T.n_elems
+    assert st["capacity"] == cfg.capacity and st["sum_dims"] == cfg.sum_dims
+
+
+def test_auto_capacity_is_smallest_power_of_two_at_half_load():
+    for n in [1, 2, 3, 1000, 65536, 65537]:
+        keys = np.arange(n, dtype=np.int64)
+        st, _, _ = E.emb_table_plan([4], "f32", keys, 0)
+        cap = st["capacity"]
+        assert cap >= 2 * n and cap & (cap - 1) == 0 and (cap // 2 < 2 * n or cap == 2)
+
+
+@pytest.mark.parametrize("keys,dims,wd,cap,err", [
+    ([1, 2, 1], [4], "f32", 8, "EMB_ERR_DUP_KEY"),
+    ([1, -1], [4], "f32", 8, "EMB_ERR_RESERVED_KEY"),
+    ([(2 << 48) | 5], [4, 4], "f32", 8, "EMB_ERR_INVALID_ARG"),   # slot field >= n_slots
+    ([1, 2, 3], [4], "f32", 4, "EMB_ERR_LOAD_FACTOR"),             # 3 keys need 8 slots
+    ([1, 2], [4], "f32", 12, "EMB_ERR_LOAD_FACTOR"),               # not a power of two
+    ([1, 2], [6], "f32", 8, "EMB_ERR_UNSUPPORTED"),                # f32 dim not multiple of 4
+    ([1, 2], [4], "f16", 8, "EMB_ERR_UNSUPPORTED"),                # f16 dim not multiple of 8
+    ([1, 2], [1024], "f32", 8, "EMB_ERR_UNSUPPORTED"),             # above EMB_MAX_DIM
+])
+def test_plan_rejects_bad_tables(keys, dims, wd, cap, err):
+    with pytest.raises(E.EmbError) as ei:
+        E.emb_table_plan(dims, wd, np.array(keys, dtype=np.int64), cap)
+    assert ei.value.name == err
+    assert E.emb_last_error()
+
+
+def test_plan_stats_count_probes():
+    # every key of a tiny table lands at probe length >= 1; the sum counts them
+    keys = (np.arange(40, dtype=np.int64) * 7919) | (1 << 48)
+    st, sk, sr = E.emb_table_plan([8, 8], "f32", keys, 128, layout=True)
+    assert st["n_keys"] == 40 and (sk != -1).sum() == 40
+    assert st["sum_probe"] >= 40 and st["max_probe"] >= 1
+    assert sorted(sr[sr >= 0].tolist()) == list(range(40))
