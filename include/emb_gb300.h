@@ -81,6 +81,7 @@ typedef enum { EMB_POOL_SUM = 0, EMB_POOL_MEAN = 1 } emb_pool;
 #define EMB_FLAG_PROBE_BOUND 1u   /* a probe ran past the table's longest cluster (corrupt table) */
 #define EMB_FLAG_BAD_OFFSETS 2u   /* CSR offsets out of [0, nnz] or decreasing; clamped */
 #define EMB_FLAG_SLOT_MISMATCH 4u /* a bag held a key of another slot; it was skipped */
+#define EMB_FLAG_BAD_ROW 8u       /* emb_table_export_rows got a row index outside [0, n_keys) */
 
 /* Limits of this implementation (EMB_ERR_UNSUPPORTED beyond them). */
 #define EMB_MAX_DIM 512            /* per-slot dim; f32 dims multiple of 4, f16 of 8 */
@@ -212,6 +213,17 @@ EMB_API emb_status emb_resolve(const emb_table* table, const int64_t* keys_d, in
  */
 EMB_API emb_status emb_table_export(const emb_table* table, int64_t* keys_out, void* values_out, float* acc_out,
                             void* stream);
+
+/*
+ * emb_table_export_rows -- partial checkpoint: the weights and accumulators of
+ * selected keys-array rows (ext_rows_d int64[n], indices into the keys array
+ * given at creation).  Outputs are device buffers laid out [n, max_dim]: row
+ * i's dim(slot) elements first, zero padding after.  Either output may be
+ * NULL.  An index outside [0, n_keys) yields a zero row and raises
+ * EMB_FLAG_BAD_ROW.  Enqueued on `stream`.
+ */
+EMB_API emb_status emb_table_export_rows(const emb_table* table, const int64_t* ext_rows_d, int64_t n,
+                                         void* values_out_d, float* acc_out_d, void* stream);
 
 /* Copy the slot layout (key and keys-array index per slot, -1 = empty) to
  * host or device int64[capacity] buffers; either may be NULL.  Synchronises. */

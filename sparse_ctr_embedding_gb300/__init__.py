@@ -22,16 +22,16 @@ __all__ = [
     "EmbError", "LibraryNotBuilt", "Table", "lib", "declared_symbols",
     "emb_table_create", "emb_table_destroy", "emb_table_get_stats", "emb_table_plan",
     "emb_lookup_fwd", "emb_bwd_workspace_size", "emb_bwd_adagrad", "emb_bwd_unique_keys",
-    "emb_resolve", "emb_table_export", "emb_table_slots", "emb_check_device_flag",
+    "emb_resolve", "emb_table_export", "emb_table_export_rows", "emb_table_slots", "emb_check_device_flag",
     "emb_status_string", "emb_last_error",
-    "EMB_FLAG_PROBE_BOUND", "EMB_FLAG_BAD_OFFSETS", "EMB_FLAG_SLOT_MISMATCH",
+    "EMB_FLAG_PROBE_BOUND", "EMB_FLAG_BAD_OFFSETS", "EMB_FLAG_SLOT_MISMATCH", "EMB_FLAG_BAD_ROW",
 ]
 
 EMB_OK = 0
 STATUS = {0: "EMB_OK", 1: "EMB_ERR_INVALID_ARG", 2: "EMB_ERR_CUDA", 3: "EMB_ERR_OOM", 4: "EMB_ERR_DUP_KEY",
           5: "EMB_ERR_RESERVED_KEY", 6: "EMB_ERR_LOAD_FACTOR", 7: "EMB_ERR_WORKSPACE",
           8: "EMB_ERR_DEVICE_FLAG", 9: "EMB_ERR_UNSUPPORTED"}
-EMB_FLAG_PROBE_BOUND, EMB_FLAG_BAD_OFFSETS, EMB_FLAG_SLOT_MISMATCH = 1, 2, 4
+EMB_FLAG_PROBE_BOUND, EMB_FLAG_BAD_OFFSETS, EMB_FLAG_SLOT_MISMATCH, EMB_FLAG_BAD_ROW = 1, 2, 4, 8
 _DTYPE = {"f32": 0, "f16": 1}
 _POOL = {"sum": 0, "mean": 1}
 
@@ -89,6 +89,7 @@ def lib():
             "emb_resolve": [_vp, _vp, _i64, _vp, _vp, _vp],
             "emb_table_export": [_vp, _vp, _vp, _vp, _vp],
             "emb_table_slots": [_vp, _vp, _vp, _vp],
+            "emb_table_export_rows": [_vp, _vp, _i64, _vp, _vp, _vp],
             "emb_check_device_flag": [_vp, _vp, ctypes.POINTER(ctypes.c_uint32)],
         }
         for name, args in sig.items():
@@ -277,6 +278,21 @@ def emb_table_export(table: Table, keys_out: Optional[torch.Tensor], values_out:
     _check(lib().emb_table_export(table.handle, _ptr(keys_out, torch.int64, "keys_out"),
                                   _ptr(values_out, wt, "values_out"), _ptr(acc_out, torch.float32, "acc_out"),
                                   _stream(stream)))
+
+
+def emb_table_export_rows(table: Table, rows: torch.Tensor, values_out: Optional[torch.Tensor] = None,
+                          acc_out: Optional[torch.Tensor] = None, stream=None) -> Tuple[torch.Tensor, torch.Tensor]:
+    """Weights/accumulators of keys-array rows as [n, max_dim] device tensors (zero padded)."""
+    n, md = rows.numel(), max(table.dims)
+    wt = torch.float16 if table.wdtype == "f16" else torch.float32
+    if values_out is None:
+        values_out = torch.empty((n, md), dtype=wt, device=rows.device)
+    if acc_out is None:
+        acc_out = torch.empty((n, md), dtype=torch.float32, device=rows.device)
+    _check(lib().emb_table_export_rows(table.handle, _cuda(rows, torch.int64, "rows"), n,
+                                       _cuda(values_out, wt, "values_out"), _cuda(acc_out, torch.float32, "acc_out"),
+                                       _stream(stream)))
+    return values_out, acc_out
 
 
 def emb_table_slots(table: Table, slot_key_out: Optional[torch.Tensor], slot_row_out: Optional[torch.Tensor],

@@ -242,6 +242,34 @@ __global__ void slots_kernel(const Slot* slots, long long p0, long long p1, long
   }
 }
 
+// Selected keys-array rows to a dense [n, max_dim] buffer (zero padded).
+template <typename T>
+__global__ void export_rows_kernel(TableView t, const unsigned* ext_to_int, const long long* __restrict__ rows,
+                                   long long n, unsigned n_keys, T* __restrict__ vout, float* __restrict__ aout) {
+  const int lane = threadIdx.x & 31;
+  const T* W = static_cast<const T*>(t.W);
+  long long i = (blockIdx.x * (long long)blockDim.x + threadIdx.x) >> 5;
+  const long long stride = ((long long)gridDim.x * blockDim.x) >> 5;
+  for (; i < n; i += stride) {
+    const long long e = rows[i];
+    const bool ok = e >= 0 && e < (long long)n_keys;
+    if (!ok && lane == 0) atomicOr(t.flags, EMB_FLAG_BAD_ROW);
+    int D = 0;
+    long long ie = 0;
+    if (ok) {
+      const unsigned r = ext_to_int[e];
+      const SlotInfo si = t.sinfo[key_slot(t.row_key[r])];
+      D = si.dim;
+      ie = row_elem(si, r);
+    }
+    for (int j = lane; j < t.max_dim; j += 32) {
+      const bool in = j < D;
+      if (vout) vout[i * t.max_dim + j] = in ? W[ie + j] : T(0);
+      if (aout) aout[i * t.max_dim + j] = in ? t.ACC[ie + j] : 0.f;
+    }
+  }
+}
+
 // Kernel P: the probe alone, one thread per key.
 __global__ void resolve_kernel(TableView t, const long long* __restrict__ keys, long long n, long long* slot_out,
                                long long* row_out) {
@@ -519,6 +547,25 @@ emb_status emb_table_export(const emb_table* table, int64_t* keys_out, void* val
     }
   }
   EMB_CUDA(cudaStreamSynchronize(st));
+  return EMB_OK;
+}
+
+emb_status emb_table_export_rows(const emb_table* table, const int64_t* ext_rows_d, int64_t n, void* values_out_d,
+                                 float* acc_out_d, void* stream) {
+  if (!table || n < 0 || (n > 0 && !ext_rows_d)) return fail(EMB_ERR_INVALID_ARG, "bad export_rows arguments");
+  if (n == 0 || (!values_out_d && !acc_out_d)) return EMB_OK;
+  cudaStream_t st = (cudaStream_t)stream;
+  const int grid = grid_for(n * 32, 256);
+  const unsigned nk = (unsigned)table->st.n_keys;
+  if (table->st.wdtype == EMB_F16)
+    export_rows_kernel<unsigned short><<<grid, 256, 0, st>>>(table->view(), table->ext_to_int_d,
+                                                             (const long long*)ext_rows_d, n, nk,
+                                                             (unsigned short*)values_out_d, acc_out_d);
+  else
+    export_rows_kernel<unsigned><<<grid, 256, 0, st>>>(table->view(), table->ext_to_int_d,
+                                                       (const long long*)ext_rows_d, n, nk, (unsigned*)values_out_d,
+                                                       acc_out_d);
+  EMB_CUDA(cudaGetLastError());
   return EMB_OK;
 }
 
