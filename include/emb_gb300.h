@@ -189,6 +189,36 @@ EMB_API emb_status emb_bwd_adagrad(emb_table* table, const int64_t* offsets_d, i
                            void* workspace_d, size_t ws_bytes, void* stream);
 
 /*
+ * emb_bwd_adagrad_noalloc -- the same backward + Adagrad step as
+ * emb_bwd_adagrad, for callers that cannot allocate device memory: code that
+ * runs under a memory manager which already owns all of the GPU's memory
+ * (for example another framework's caching allocator), or a latency-critical
+ * loop whose rules forbid allocation during a step.  The pages have no
+ * counterpart of this entry point; it exists only for such callers.
+ * Instead of a caller workspace it uses one scratch array that the library
+ * holds in device memory, EMB_NOALLOC_SCRATCH_BYTES long, on every GPU that
+ * loads the library, until the process exits.  The call allocates nothing.
+ *   - A batch whose workspace (emb_bwd_workspace_size) exceeds
+ *     EMB_NOALLOC_SCRATCH_BYTES is rejected with EMB_ERR_UNSUPPORTED before
+ *     any work is queued (about 3 million lookups fit at dim 128).
+ *   - The first call on a device looks up the array's device address once
+ *     (cudaGetSymbolAddress, with that device current); make that first call
+ *     before any stream capture.
+ *   - Every call on a device shares the one array and leaves its contents
+ *     behind.  Calls that can overlap on the GPU (different streams without
+ *     ordering, or several threads) race on it and give wrong results: order
+ *     them.  No part of the array has to start at zero; each call writes
+ *     every region before reading it.
+ *   - emb_bwd_unique_keys cannot read this array; use emb_bwd_adagrad with a
+ *     workspace when the unique keys are needed.
+ * Arguments and errors otherwise as emb_bwd_adagrad.
+ */
+#define EMB_NOALLOC_SCRATCH_BYTES (64u << 20)
+EMB_API emb_status emb_bwd_adagrad_noalloc(emb_table* table, const int64_t* offsets_d, int64_t n_bags,
+                                           const int64_t* keys_d, int64_t nnz, emb_pool pool,
+                                           const float* grad_out_d, float lr, float eps, void* stream);
+
+/*
  * emb_bwd_unique_keys -- the deduplicated key set of the last emb_bwd_adagrad
  * that used this workspace.  keys_out_d int64[>= nnz of that call] receives
  * the unique hit keys (slot-major internal row order); n_unique_d int64[1]

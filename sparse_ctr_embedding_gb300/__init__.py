@@ -21,7 +21,8 @@ from .build import HEADER, LIB_PATH, build
 __all__ = [
     "EmbError", "LibraryNotBuilt", "Table", "lib", "declared_symbols",
     "emb_table_create", "emb_table_destroy", "emb_table_get_stats", "emb_table_plan",
-    "emb_lookup_fwd", "emb_bwd_workspace_size", "emb_bwd_adagrad", "emb_bwd_unique_keys",
+    "emb_lookup_fwd", "emb_bwd_workspace_size", "emb_bwd_adagrad", "emb_bwd_adagrad_noalloc",
+    "emb_bwd_unique_keys", "EMB_NOALLOC_SCRATCH_BYTES",
     "emb_resolve", "emb_table_export", "emb_table_export_rows", "emb_table_slots", "emb_check_device_flag",
     "emb_status_string", "emb_last_error",
     "EMB_FLAG_PROBE_BOUND", "EMB_FLAG_BAD_OFFSETS", "EMB_FLAG_SLOT_MISMATCH", "EMB_FLAG_BAD_ROW",
@@ -32,6 +33,7 @@ STATUS = {0: "EMB_OK", 1: "EMB_ERR_INVALID_ARG", 2: "EMB_ERR_CUDA", 3: "EMB_ERR_
           5: "EMB_ERR_RESERVED_KEY", 6: "EMB_ERR_LOAD_FACTOR", 7: "EMB_ERR_WORKSPACE",
           8: "EMB_ERR_DEVICE_FLAG", 9: "EMB_ERR_UNSUPPORTED"}
 EMB_FLAG_PROBE_BOUND, EMB_FLAG_BAD_OFFSETS, EMB_FLAG_SLOT_MISMATCH, EMB_FLAG_BAD_ROW = 1, 2, 4, 8
+EMB_NOALLOC_SCRATCH_BYTES = 64 << 20
 _DTYPE = {"f32": 0, "f16": 1}
 _POOL = {"sum": 0, "mean": 1}
 
@@ -86,6 +88,8 @@ def lib():
             "emb_bwd_adagrad": [_vp, _vp, _i64, _vp, _i64, ctypes.c_int, _vp, ctypes.c_float, ctypes.c_float,
                                 _vp, ctypes.c_size_t, _vp],
             "emb_bwd_unique_keys": [_vp, _vp, ctypes.c_size_t, _vp, _vp, _vp],
+            "emb_bwd_adagrad_noalloc": [_vp, _vp, _i64, _vp, _i64, ctypes.c_int, _vp, ctypes.c_float,
+                                        ctypes.c_float, _vp],
             "emb_resolve": [_vp, _vp, _i64, _vp, _vp, _vp],
             "emb_table_export": [_vp, _vp, _vp, _vp, _vp],
             "emb_table_slots": [_vp, _vp, _vp, _vp],
@@ -250,6 +254,17 @@ def emb_bwd_adagrad(table: Table, offsets: torch.Tensor, keys: torch.Tensor, poo
                                  _cuda(grad_out, torch.float32, "grad_out"), ctypes.c_float(lr),
                                  ctypes.c_float(eps), _cuda(workspace, None, "workspace"),
                                  workspace.numel() * workspace.element_size(), _stream(stream)))
+
+
+def emb_bwd_adagrad_noalloc(table: Table, offsets: torch.Tensor, keys: torch.Tensor, pool: str,
+                            grad_out: torch.Tensor, lr: float, eps: float, stream=None) -> None:
+    """emb_bwd_adagrad without a workspace: for callers that cannot allocate
+    device memory, it uses the library's fixed EMB_NOALLOC_SCRATCH_BYTES scratch
+    (shared by every call on the device: order overlapping calls)."""
+    _check(lib().emb_bwd_adagrad_noalloc(table.handle, _cuda(offsets, torch.int64, "offsets"), offsets.numel() - 1,
+                                         _cuda(keys, torch.int64, "keys"), keys.numel(), _POOL[pool],
+                                         _cuda(grad_out, torch.float32, "grad_out"), ctypes.c_float(lr),
+                                         ctypes.c_float(eps), _stream(stream)))
 
 
 def emb_bwd_unique_keys(table: Table, workspace: torch.Tensor, keys_out: torch.Tensor, n_unique_out: torch.Tensor,

@@ -32,6 +32,8 @@
 // with IEEE sqrt and division (no fast-math), half weights rounded to
 // nearest-even on store.
 #include <algorithm>
+#include <cstdio>
+#include <mutex>
 
 #include "emb_internal.cuh"
 
@@ -748,11 +750,56 @@ static emb_status run_bwd(emb_table* table, const int64_t* offsets_d, int64_t n_
   return EMB_OK;
 }
 
+// Scratch for emb_bwd_adagrad_noalloc, for callers that cannot allocate
+// device memory.  The loader reserves it on every GPU that loads this library;
+// host code must not pass the symbol itself to a kernel (on the host it only
+// names a stand-in), so each device's address is looked up once.
+static __device__ __align__(256) unsigned char g_noalloc_scratch[EMB_NOALLOC_SCRATCH_BYTES];
+
+constexpr int kMaxDevices = 64;
+static std::mutex g_noalloc_mu;
+static void* g_noalloc_ptr[kMaxDevices] = {};
+
+static emb_status noalloc_scratch(void** out) {
+  int dev = 0;
+  EMB_CUDA(cudaGetDevice(&dev));
+  if (dev < 0 || dev >= kMaxDevices) return fail(EMB_ERR_UNSUPPORTED, "device index beyond the no-alloc table");
+  std::lock_guard<std::mutex> g(g_noalloc_mu);
+  if (!g_noalloc_ptr[dev]) {
+    void* p = nullptr;
+    cudaError_t e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaGetSymbolAddress(no-alloc scratch)");
+    g_noalloc_ptr[dev] = p;
+  }
+  *out = g_noalloc_ptr[dev];
+  return EMB_OK;
+}
+
 }  // namespace emb
 
 using namespace emb;
 
 extern "C" {
+
+emb_status emb_bwd_adagrad_noalloc(emb_table* table, const int64_t* offsets_d, int64_t n_bags, const int64_t* keys_d,
+                                   int64_t nnz, emb_pool pool, const float* grad_out_d, float lr, float eps,
+                                   void* stream) {
+  emb_status rc = check_batch(table, offsets_d, n_bags, keys_d, nnz, pool);
+  if (rc != EMB_OK) return rc;
+  if (n_bags > 0 && !grad_out_d) return fail(EMB_ERR_INVALID_ARG, "grad_out is NULL");
+  const WsLayout L = ws_layout(table, n_bags, nnz);
+  if (L.total > (size_t)EMB_NOALLOC_SCRATCH_BYTES) {
+    char buf[192];
+    std::snprintf(buf, sizeof buf,
+                  "batch needs %zu bytes of scratch; emb_bwd_adagrad_noalloc holds %u (use emb_bwd_adagrad "
+                  "with a workspace)", L.total, (unsigned)EMB_NOALLOC_SCRATCH_BYTES);
+    return fail(EMB_ERR_UNSUPPORTED, buf);
+  }
+  void* scratch = nullptr;
+  if ((rc = noalloc_scratch(&scratch)) != EMB_OK) return rc;
+  return run_bwd(table, offsets_d, n_bags, keys_d, nnz, pool, grad_out_d, lr, eps, (char*)scratch, L,
+                 (cudaStream_t)stream);
+}
 
 emb_status emb_bwd_workspace_size(const emb_table* table, int64_t n_bags, int64_t nnz, size_t* bytes) {
   if (!table || !bytes || n_bags < 0 || nnz < 0) return fail(EMB_ERR_INVALID_ARG, "bad workspace query");
