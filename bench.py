@@ -36,6 +36,8 @@ def parse():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--config", type=int, default=5, help="workload 1..5")
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--vocab-div", type=int, default=1, help="shrink keys per slot (profiling a small case)")
+    ap.add_argument("--batch-div", type=int, default=1, help="shrink the batch (profiling a small case)")
     ap.add_argument("--cpu-samples", type=int, default=2048,
                     help="samples of the batch the CPU-baseline oracle runs (bounded sample)")
     ap.add_argument("--ref-samples", type=int, default=128, help="samples per reference-arm step")
@@ -136,7 +138,7 @@ def max_over_ranks(ws, x: float) -> float:
 def launches_per_step(n_keys: int) -> int:
     """Kernels this library launches for one fwd + one bwd call."""
     bits = max(1, int(n_keys).bit_length())
-    passes = max(1, math.ceil(bits / 8))
+    passes = max(1, math.ceil(bits / 9))
     return 1 + 1 + passes * 5 + 2   # fwd; expand; (count + 3 scan + scatter) per radix pass; reduce; fixup
 
 
@@ -259,6 +261,8 @@ def run_ours(args):
     barrier(ws)
     E.build()
     cfg = W.config(args.config)
+    if args.vocab_div > 1 or args.batch_div > 1:
+        cfg = W.scaled(cfg, args.vocab_div, args.batch_div)
     stream = torch.cuda.current_stream()
 
     # ---- workload (generated on the device, keys copied to the host for the table build)

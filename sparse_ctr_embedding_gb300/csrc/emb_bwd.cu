@@ -29,7 +29,8 @@
 // No float atomics: every sum has a fixed order, so the step is bitwise
 // reproducible.  The Adagrad arithmetic per element, in float32:
 //   g = G;  acc += g * g;  w -= lr * g / (sqrt(acc) + eps)
-// with IEEE sqrt and division (no fast-math), half weights rounded to
+// with sqrt and the quotient from the hardware reciprocal square root and
+// reciprocal (a few ulp; see adagrad_elem), half weights rounded to
 // nearest-even on store.
 #include <algorithm>
 #include <cstdio>
@@ -42,12 +43,12 @@ namespace emb {
 emb_status check_batch(const emb_table* t, const int64_t* offsets_d, int64_t n_bags, const int64_t* keys_d,
                        int64_t nnz, int pool);
 
-constexpr int kChunk = 256;                      // sorted positions per reduce chunk
+constexpr int kChunk = 512;                      // sorted positions per reduce sub-chunk
 constexpr int kSortWarps = 8;
 constexpr int kSortThreads = kSortWarps * 32;
 constexpr int kSortItems = 16;                   // keys per lane per tile
 constexpr int kSortTile = kSortThreads * kSortItems;
-constexpr int kRadixBits = 8;
+constexpr int kRadixBits = 9;                    // 27-bit rows (100M) sort in 3 passes
 constexpr int kDigits = 1 << kRadixBits;
 constexpr int kScanThreads = 256;
 constexpr int kScanItems = 16;
@@ -412,6 +413,17 @@ __device__ __forceinline__ void stw4(__half* p, const float (&v)[4]) {
   *reinterpret_cast<uint2*>(p) = x;
 }
 
+// One element of the Adagrad update:  acc += g*g;  w -= lr*g / (sqrt(acc) + eps).
+// sqrt(acc) is acc * rsqrt(acc) and the quotient a fast divide (hardware
+// reciprocal square root and reciprocal, each within a few ulp), which keeps
+// the update well inside the float32 tolerance at a fraction of the
+// instructions of the correctly rounded sequences.
+__device__ __forceinline__ void adagrad_elem(float& w, float& a, float g, float lr, float eps) {
+  a = fmaf(g, g, a);
+  const float sq = a > 0.f ? a * rsqrtf(a) : 0.f;
+  w -= __fdividef(lr * g, sq + eps);
+}
+
 // Element-wise Adagrad on one lane's columns of one row.
 template <typename TW, int NCB>
 __device__ __forceinline__ void adagrad_row(const TableView& t, long long e0, int D, int G, int li,
@@ -426,11 +438,7 @@ __device__ __forceinline__ void adagrad_row(const TableView& t, long long e0, in
       float wv[4];
       ldw4(W + e0 + ce, wv);
 #pragma unroll
-      for (int j = 0; j < 4; ++j) {
-        const float gj = g[c][j];
-        av[j] = av[j] + gj * gj;
-        wv[j] = wv[j] - (lr * gj) / (sqrtf(av[j]) + eps);
-      }
+      for (int j = 0; j < 4; ++j) adagrad_elem(wv[j], av[j], g[c][j], lr, eps);
       *reinterpret_cast<float4*>(t.ACC + e0 + ce) = make_float4(av[0], av[1], av[2], av[3]);
       stw4(W + e0 + ce, wv);
     }
@@ -452,101 +460,279 @@ __device__ __forceinline__ void row_geom(const TableView& t, unsigned row, int& 
   }
 }
 
-template <typename TW, int G, int NCB, int U>
-__global__ void __launch_bounds__(256) segreduce_adagrad_kernel(
+// Element-wise Adagrad on VW consecutive columns starting at element e (VW a
+// multiple of 4).
+template <typename TW, int VW>
+__device__ __forceinline__ void adagrad_cols(const TableView& t, long long e, const float* g, float lr, float eps) {
+  TW* W = static_cast<TW*>(t.W);
+#pragma unroll
+  for (int h = 0; h < VW; h += 4) {
+    const float4 a = *reinterpret_cast<const float4*>(t.ACC + e + h);
+    float av[4] = {a.x, a.y, a.z, a.w};
+    float wv[4];
+    ldw4(W + e + h, wv);
+#pragma unroll
+    for (int j = 0; j < 4; ++j) adagrad_elem(wv[j], av[j], g[h + j], lr, eps);
+    *reinterpret_cast<float4*>(t.ACC + e + h) = make_float4(av[0], av[1], av[2], av[3]);
+    stw4(W + e + h, wv);
+  }
+}
+
+// Geometry of a row taken from the feature slot of a bag that holds it (the
+// expand step only pairs a row with bags of its own slot).  ok is false for a
+// row outside that slot's range, which only stale workspace data can produce.
+struct RowGeo {
+  long long e0;
+  int D;
+  int col;
+  bool ok;
+};
+
+__device__ __forceinline__ RowGeo geo_from_slot(const TableView& t, unsigned row, int s) {
+  RowGeo g;
+  if (t.uniform_dim) {
+    g.D = t.uniform_dim;
+    g.col = s * g.D;
+    g.ok = row < t.n_rows;
+    g.e0 = (long long)row * g.D;
+  } else {
+    const SlotInfo si = t.sinfo[s];
+    g.D = si.dim;
+    g.col = si.col;
+    g.ok = row >= si.row_base && row - si.row_base < si.n_rows;
+    g.e0 = g.ok ? row_elem(si, row) : 0;
+  }
+  return g;
+}
+
+__device__ __forceinline__ void prefetch_l2(const void* p) { asm volatile("prefetch.global.L2 [%0];" ::"l"(p)); }
+
+// The weight and accumulator bytes of a row, pulled towards L2 ahead of its
+// read-modify-write.
+template <typename TW>
+__device__ __forceinline__ void prefetch_row(const TableView& t, const RowGeo& g) {
+  const char* w = reinterpret_cast<const char*>(static_cast<const TW*>(t.W) + g.e0);
+  const char* a = reinterpret_cast<const char*>(t.ACC + g.e0);
+  for (int o = 0; o < g.D * (int)sizeof(TW); o += 128) prefetch_l2(w + o);
+  for (int o = 0; o < g.D * 4; o += 128) prefetch_l2(a + o);
+}
+
+// VW consecutive floats of grad_out: one 16- or 32-byte read-only load.
+template <int VW>
+struct GradVec;
+template <>
+struct GradVec<4> {
+  float v[4];
+  __device__ __forceinline__ void load(const float* p) {
+    const float4 x = __ldg(reinterpret_cast<const float4*>(p));
+    v[0] = x.x; v[1] = x.y; v[2] = x.z; v[3] = x.w;
+  }
+};
+template <>
+struct GradVec<8> {
+  float v[8];
+  __device__ __forceinline__ void load(const float* p) {
+    asm("ld.global.nc.v8.f32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%8];"
+        : "=f"(v[0]), "=f"(v[1]), "=f"(v[2]), "=f"(v[3]), "=f"(v[4]), "=f"(v[5]), "=f"(v[6]), "=f"(v[7])
+        : "l"(p));
+  }
+};
+
+// acc[i] += w * g[i] for an even count, two lanes of fp32 per instruction.
+template <int N>
+__device__ __forceinline__ void fma_x2(float* acc, float w, const float* g) {
+#pragma unroll
+  for (int i = 0; i < N; i += 2) {
+    unsigned long long a, x, ww, r;
+    asm("mov.b64 %0, {%1,%2};" : "=l"(a) : "f"(acc[i]), "f"(acc[i + 1]));
+    asm("mov.b64 %0, {%1,%2};" : "=l"(x) : "f"(g[i]), "f"(g[i + 1]));
+    asm("mov.b64 %0, {%1,%1};" : "=l"(ww) : "f"(w));
+    asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(r) : "l"(ww), "l"(x), "l"(a));
+    asm("mov.b64 {%0,%1}, %2;" : "=f"(acc[i]), "=f"(acc[i + 1]) : "l"(r));
+  }
+}
+
+struct StageMeta {
+  long long e0;
+  unsigned row;
+  int D;
+  int flags;  // bit0: segment starts in this sub-chunk, bit1: ends in it
+};
+
+// One lane group of G lanes streams a sub-chunk of kChunk sorted positions;
+// each lane owns VW-float column vectors (NCB of them) of the row.  Per
+// window of G positions the lanes first work in parallel, one position each:
+// row, bag, merged run of equal (row, bag) neighbours, its weight (1/L times
+// the run length), the index of its grad_out row, and whether a new row
+// starts there; lanes that start a row prefetch its weights and
+// accumulators into L2.  The group then walks the window in order, U
+// positions at a time: one shuffle and one vector load per position and
+// lane, packed multiply-adds, and at a row start the finished row is staged
+// in shared memory.  Staged rows are then applied (Adagrad on a whole
+// segment) or parked (partial of a segment cut by a sub-chunk edge) by one
+// copy of that code, outside the unrolled walk.
+constexpr int kRedWarps = 4;  // warps per reduce block
+
+template <typename TW, int G, int VW, int NCB, int U>
+__global__ void __launch_bounds__(kRedWarps * 32) segreduce_adagrad_kernel(
     TableView t, const unsigned* __restrict__ K, const unsigned* __restrict__ V, const float* __restrict__ scale,
-    int mean, const float* __restrict__ grad, unsigned n, unsigned n_bags, unsigned n_chunks, float* __restrict__ partA,
-    float* __restrict__ partB, unsigned* __restrict__ arow, float lr, float eps) {
+    int mean, const float* __restrict__ grad, unsigned n, unsigned n_bags, unsigned n_chunks,
+    float* __restrict__ partA, float* __restrict__ partB, unsigned* __restrict__ arow, float lr, float eps) {
   constexpr int P = 32 / G;
-  __shared__ unsigned piece_start[8][kChunk + 1];
-  const int w = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  constexpr int CW = G * VW * NCB;      // columns a group covers
+  constexpr int kStage = U + 1;
+  constexpr unsigned kSkip = 0xFFFFFFFFu;
+  __shared__ __align__(16) float stage[kRedWarps][P][kStage][CW];
+  __shared__ StageMeta meta[kRedWarps][P][kStage];
+  const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
   const int sub = lane / G, li = lane % G;
-  const unsigned miss = t.n_rows;
+  const unsigned gmask = G == 32 ? 0xffffffffu : (((1u << G) - 1u) << (sub * G));
+  const unsigned gbits = G == 32 ? 0xffffffffu : ((1u << G) - 1u);
   const unsigned S = (unsigned)t.n_slots;
+  const unsigned miss = t.n_rows;
   const int maxd = t.max_dim;
-  unsigned* ps = piece_start[w];
-  const unsigned nwarps = (gridDim.x * blockDim.x) >> 5;
-  for (unsigned c = (blockIdx.x * blockDim.x + threadIdx.x) >> 5; c < n_chunks; c += nwarps) {
+  const int udim = t.uniform_dim;
+  float(*st)[CW] = stage[wid][sub];
+  StageMeta* mt = meta[wid][sub];
+  const unsigned n_groups = ((gridDim.x * blockDim.x) >> 5) * P;
+  for (unsigned c = ((blockIdx.x * blockDim.x + threadIdx.x) >> 5) * P + sub; c < n_chunks; c += n_groups) {
     const unsigned cs = c * kChunk;
     const unsigned ce = min(cs + kChunk, n);
-    // piece starts: cs and every position where the row changes
-    unsigned np = 0;
-    unsigned prev = cs > 0 ? K[cs - 1] : kNoRow;
-    for (unsigned j0 = cs; j0 < ce; j0 += 32) {
-      const unsigned i = j0 + lane;
-      const unsigned k = i < ce ? K[i] : kNoRow;
-      unsigned kp = __shfl_up_sync(0xffffffffu, k, 1);
-      if (lane == 0) kp = prev;
-      prev = __shfl_sync(0xffffffffu, k, 31);
-      const bool st = i < ce && (i == cs || k != kp);
-      const unsigned m = __ballot_sync(0xffffffffu, st);
-      if (st) ps[np + __popc(m & lanemask_lt())] = i;
-      np += __popc(m);
-    }
-    if (lane == 0) ps[np] = ce;
-    if (lane == 0) arow[c] = kNoRow;
-    __syncwarp();
-    const bool first_starts = cs == 0 || K[cs - 1] != K[cs];
+    const unsigned before = cs > 0 ? K[cs - 1] : kNoRow;
+    const bool first_starts = K[cs] != before;
     const bool last_ends = ce >= n || K[ce] != K[ce - 1];
-    for (unsigned p = sub; p < np; p += P) {
-      const unsigned a = ps[p], b = ps[p + 1];
-      const unsigned row = K[a];
-      if (row >= miss) continue;  // misses (and anything past the table) sort last
-      int D, col;
-      long long e0;
-      row_geom(t, row, D, col, e0);
-      float acc[NCB][4];
+    if (li == 0) arow[c] = kNoRow;
+    unsigned cur = kNoRow;
+    bool cur_starts = first_starts;
+    RowGeo cg{0, 0, 0, false};
+    float acc[NCB][VW];
+#pragma unroll
+    for (int cc = 0; cc < NCB; ++cc)
+#pragma unroll
+      for (int j = 0; j < VW; ++j) acc[cc][j] = 0.f;
+
+    // stage the finished row `cur` (no-op for misses and stale rows)
+    auto stage_cur = [&](int slot, bool ends) {
 #pragma unroll
       for (int cc = 0; cc < NCB; ++cc)
 #pragma unroll
-        for (int j = 0; j < 4; ++j) acc[cc][j] = 0.f;
-      for (unsigned i0 = a; i0 < b; i0 += U) {
-        float4 gv[U][NCB];
-        float sc[U];
-#pragma unroll
-        for (int u = 0; u < U; ++u) {
-          const unsigned i = i0 + u;
-          unsigned bag = i < b ? V[i] : 0;
-          const bool ok = i < b && bag < n_bags;
-          bag = ok ? bag : 0;
-          sc[u] = ok ? (mean ? scale[bag] : 1.f) : 0.f;
-          const float* gp = grad + (size_t)(bag / S) * t.sum_dims + col;
+        for (int j = 0; j < VW; j += 4)
+          *reinterpret_cast<float4*>(&st[slot][(cc * G + li) * VW + j]) =
+              make_float4(acc[cc][j], acc[cc][j + 1], acc[cc][j + 2], acc[cc][j + 3]);
+      if (li == 0) mt[slot] = StageMeta{cg.e0, cur, (cur < miss && cg.ok) ? cg.D : 0,
+                                        (cur_starts ? 1 : 0) | (ends ? 2 : 0)};
+    };
+    // apply or park the staged rows [0, ns)
+    auto drain = [&](int ns) {
+      __syncwarp(gmask);
+      for (int f = 0; f < ns; ++f) {
+        const StageMeta sm = mt[f];
+        if (sm.D == 0) continue;
+        if (sm.flags == 3) {
 #pragma unroll
           for (int cc = 0; cc < NCB; ++cc) {
-            const int cidx = (cc * G + li) * 4;
-            gv[u][cc] = (ok && cidx < D) ? __ldg(reinterpret_cast<const float4*>(gp + cidx))
-                                          : make_float4(0.f, 0.f, 0.f, 0.f);
+            const int col = (cc * G + li) * VW;
+            if (col < sm.D) adagrad_cols<TW, VW>(t, sm.e0 + col, &st[f][col], lr, eps);
           }
-        }
+        } else {
+          float* dst = ((sm.flags & 1) ? partA : partB) + (size_t)c * maxd;
+          if ((sm.flags & 1) && li == 0) arow[c] = sm.row;
 #pragma unroll
-        for (int u = 0; u < U; ++u) {
-          if (i0 + u < b) {
+          for (int cc = 0; cc < NCB; ++cc) {
+            const int col = (cc * G + li) * VW;
+            if (col < sm.D) {
 #pragma unroll
-            for (int cc = 0; cc < NCB; ++cc) {
-              acc[cc][0] += sc[u] * gv[u][cc].x;
-              acc[cc][1] += sc[u] * gv[u][cc].y;
-              acc[cc][2] += sc[u] * gv[u][cc].z;
-              acc[cc][3] += sc[u] * gv[u][cc].w;
+              for (int j = 0; j < VW; j += 4)
+                *reinterpret_cast<float4*>(dst + col + j) = *reinterpret_cast<const float4*>(&st[f][col + j]);
             }
           }
         }
       }
-      const bool starts = p > 0 || first_starts;
-      const bool ends = p + 1 < np || last_ends;
-      if (starts && ends) {
-        adagrad_row<TW, NCB>(t, e0, D, G, li, acc, lr, eps);
-      } else {
-        float* dst = (starts ? partA : partB) + (size_t)c * maxd;
-        if (starts && li == 0) arow[c] = row;
-#pragma unroll
-        for (int cc = 0; cc < NCB; ++cc) {
-          const int cidx = (cc * G + li) * 4;
-          if (cidx < D)
-            *reinterpret_cast<float4*>(dst + cidx) = make_float4(acc[cc][0], acc[cc][1], acc[cc][2], acc[cc][3]);
+      __syncwarp(gmask);
+    };
+
+    unsigned prev_row = before;
+    for (unsigned i0 = cs; i0 < ce; i0 += G) {
+      // ---- lane-parallel bookkeeping, one position per lane
+      const int m = (int)min((unsigned)G, ce - i0);
+      const bool valid = li < m;
+      const unsigned kk = valid ? K[i0 + li] : kNoRow;
+      const unsigned vv = valid ? V[i0 + li] : 0u;
+      unsigned kp = __shfl_up_sync(gmask, kk, 1, G);
+      const unsigned vp = __shfl_up_sync(gmask, vv, 1, G);
+      if (li == 0) kp = prev_row;
+      prev_row = __shfl_sync(gmask, kk, m - 1, G);
+      const bool dup = valid && li > 0 && kk == kp && vv == vp;
+      const unsigned dm = (__ballot_sync(gmask, dup) >> (sub * G)) & gbits;
+      const unsigned above = li + 1 < 32 ? (~dm) & ~((2u << li) - 1u) : 0u;
+      const int nxt = min(above ? __ffs(above) - 1 : G, m);
+      const bool use = valid && !dup && kk < miss && vv < n_bags;
+      const bool start = valid && (kk != kp || (i0 == cs && li == 0));
+      const unsigned smask = (__ballot_sync(gmask, start) >> (sub * G)) & gbits;
+      int sj = 0, Dj = udim;
+      unsigned go = kSkip;  // index, in VW-float vectors, of this position's grad_out columns
+      if (use) {
+        if (udim) {
+          go = vv * (unsigned)(udim / VW);   // (b*S + s) * D = b * sum_dims + s * D
+        } else {
+          sj = (int)(vv % S);
+          const SlotInfo si = t.sinfo[sj];
+          Dj = si.dim;
+          go = (unsigned)(((unsigned long long)(vv / S) * (unsigned)t.sum_dims + (unsigned)si.col) / VW);
         }
       }
+      const float w = use ? (mean ? scale[vv] : 1.f) * (float)(nxt - li) : 0.f;
+      if (use && start) {
+        const RowGeo g = geo_from_slot(t, kk, sj);
+        if (g.ok) prefetch_row<TW>(t, g);
+      }
+      // ---- in-order walk, U positions in flight per lane
+      for (int j0 = 0; j0 < m; j0 += U) {
+        GradVec<VW> gv[U][NCB];
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+          const int src = (j0 + u) & (G - 1);
+          const unsigned gj = __shfl_sync(gmask, go, src, G);
+          const int dj = udim ? udim : __shfl_sync(gmask, Dj, src, G);
+          const bool live = j0 + u < m && gj != kSkip;
+#pragma unroll
+          for (int cc = 0; cc < NCB; ++cc) {
+            const int q = cc * G + li;
+            if (live && q * VW < dj) {
+              gv[u][cc].load(grad + ((size_t)gj + q) * VW);
+            } else {
+#pragma unroll
+              for (int j = 0; j < VW; ++j) gv[u][cc].v[j] = 0.f;
+            }
+          }
+        }
+        int ns = 0;
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+          const int j = j0 + u;
+          if (j >= m) break;
+          if ((smask >> j) & 1u) {
+            if (cur != kNoRow) stage_cur(ns++, true);
+            cur = __shfl_sync(gmask, kk, j, G);
+            const unsigned bag = __shfl_sync(gmask, vv, j, G);
+            cur_starts = (i0 + j > cs) || first_starts;
+            cg = (cur < miss && bag < n_bags) ? geo_from_slot(t, cur, (int)(bag % S)) : RowGeo{0, 0, 0, false};
+#pragma unroll
+            for (int cc = 0; cc < NCB; ++cc)
+#pragma unroll
+              for (int q = 0; q < VW; ++q) acc[cc][q] = 0.f;
+          }
+          const float wj = __shfl_sync(gmask, w, j, G);
+#pragma unroll
+          for (int cc = 0; cc < NCB; ++cc) fma_x2<VW>(acc[cc], wj, gv[u][cc].v);
+        }
+        if (ns) drain(ns);
+      }
     }
-    __syncwarp();
+    if (cur != kNoRow) {
+      stage_cur(0, last_ends);
+      drain(1);
+    }
   }
 }
 
@@ -583,17 +769,29 @@ __global__ void __launch_bounds__(256) fixup_kernel(TableView t, const unsigned*
     for (int cc = 0; cc < NCB; ++cc)
 #pragma unroll
       for (int j = 0; j < 4; ++j) acc[cc][j] = 0.f;
-    for (unsigned j = j0; j < j1; ++j) {
-      const float* src = (j == 0 ? partA + (size_t)c * maxd : partB + (size_t)(c + j) * maxd);
+    for (unsigned jb = j0; jb < j1; jb += 4) {
+      float4 x[4][NCB];
 #pragma unroll
-      for (int cc = 0; cc < NCB; ++cc) {
-        const int cidx = (cc * G + li) * 4;
-        if (cidx < D) {
-          const float4 x = *reinterpret_cast<const float4*>(src + cidx);
-          acc[cc][0] += x.x;
-          acc[cc][1] += x.y;
-          acc[cc][2] += x.z;
-          acc[cc][3] += x.w;
+      for (int q = 0; q < 4; ++q) {
+        const unsigned j = jb + q;
+        const float* src = (j == 0 ? partA + (size_t)c * maxd : partB + (size_t)(c + j) * maxd);
+#pragma unroll
+        for (int cc = 0; cc < NCB; ++cc) {
+          const int cidx = (cc * G + li) * 4;
+          x[q][cc] = (j < j1 && cidx < D) ? *reinterpret_cast<const float4*>(src + cidx)
+                                          : make_float4(0.f, 0.f, 0.f, 0.f);
+        }
+      }
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        if (jb + q < j1) {
+#pragma unroll
+          for (int cc = 0; cc < NCB; ++cc) {
+            acc[cc][0] += x[q][cc].x;
+            acc[cc][1] += x[q][cc].y;
+            acc[cc][2] += x[q][cc].z;
+            acc[cc][3] += x[q][cc].w;
+          }
         }
       }
     }
@@ -661,37 +859,61 @@ static size_t scatter_smem() {
   return sizeof(unsigned) * ((size_t)kSortWarps * kDigits + 2 * kDigits + 33 + 2 * (size_t)kSortTile);
 }
 
-template <typename TW, int G, int NCB>
+template <typename TW, int G, int VW, int NCB>
 static cudaError_t launch_reduce(const emb_table* t, const unsigned* K, const unsigned* V, const float* scale,
                                  int mean, const float* grad, unsigned n, unsigned n_bags, const WsLayout& L, char* ws,
                                  float lr, float eps, cudaStream_t st) {
-  constexpr int U = NCB >= 4 ? 2 : 4;
+  constexpr int U = (VW == 8 ? 4 : 8) / NCB;  // 128 bytes of grad_out in flight per lane
+  constexpr int P = 32 / G;
   TableView v = t->view();
-  const int threads = 256;
-  long long blocks = ((long long)L.n_chunks * 32 + threads - 1) / threads;
-  blocks = std::min<long long>(blocks, resident_blocks(threads));
+  const int threads = kRedWarps * 32;
+  int per_sm = 0;
+  cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, segreduce_adagrad_kernel<TW, G, VW, NCB, U>, threads, 0);
+  long long blocks = ((long long)L.n_chunks + (threads / 32) * P - 1) / ((threads / 32) * P);
+  blocks = std::min<long long>(blocks, (long long)std::max(1, per_sm) * sm_count());
   float* pa = (float*)(ws + L.partA);
   float* pb = (float*)(ws + L.partB);
   unsigned* ar = (unsigned*)(ws + L.arow);
-  segreduce_adagrad_kernel<TW, G, NCB, U><<<(int)std::max(1LL, blocks), threads, 0, st>>>(
+  segreduce_adagrad_kernel<TW, G, VW, NCB, U><<<(int)std::max(1LL, blocks), threads, 0, st>>>(
       v, K, V, scale, mean, grad, n, n_bags, L.n_chunks, pa, pb, ar, lr, eps);
-  fixup_kernel<TW, G, NCB><<<(int)std::max(1LL, blocks), threads, 0, st>>>(v, K, n, L.n_chunks, pa, pb, ar, lr, eps);
+  // the fixup reads partial rows four columns per lane
+  constexpr int G4 = G * VW / 4 > 32 ? 32 : G * VW / 4;
+  constexpr int NCB4 = (G * VW * NCB) / (4 * G4);
+  long long fblocks = std::min<long long>(((long long)L.n_chunks * 32 + 255) / 256, resident_blocks(256));
+  fixup_kernel<TW, G4, NCB4><<<(int)std::max(1LL, fblocks), 256, 0, st>>>(v, K, n, L.n_chunks, pa, pb, ar, lr,
+                                                                              eps);
   return cudaGetLastError();
 }
 
+// Lanes per row: one vector of VW grad_out floats per lane (32-byte vectors
+// when every dim and the grad_out pointer allow it), up to 32 lanes; wider
+// rows give each lane several column blocks.
 template <typename TW>
 static cudaError_t dispatch_reduce(const emb_table* t, const unsigned* K, const unsigned* V, const float* scale,
                                    int mean, const float* grad, unsigned n, unsigned n_bags, const WsLayout& L,
                                    char* ws, float lr, float eps, cudaStream_t st) {
-  const int vecs = t->st.max_dim / 4;  // float4 columns of the widest row
-  if (vecs <= 1) return launch_reduce<TW, 1, 1>(t, K, V, scale, mean, grad, n, n_bags, L, ws, lr, eps, st);
-  if (vecs <= 2) return launch_reduce<TW, 2, 1>(t, K, V, scale, mean, grad, n, n_bags, L, ws, lr, eps, st);
-  if (vecs <= 4) return launch_reduce<TW, 4, 1>(t, K, V, scale, mean, grad, n, n_bags, L, ws, lr, eps, st);
-  if (vecs <= 8) return launch_reduce<TW, 8, 1>(t, K, V, scale, mean, grad, n, n_bags, L, ws, lr, eps, st);
-  if (vecs <= 16) return launch_reduce<TW, 8, 2>(t, K, V, scale, mean, grad, n, n_bags, L, ws, lr, eps, st);
-  if (vecs <= 32) return launch_reduce<TW, 8, 4>(t, K, V, scale, mean, grad, n, n_bags, L, ws, lr, eps, st);
-  if (vecs <= 64) return launch_reduce<TW, 8, 8>(t, K, V, scale, mean, grad, n, n_bags, L, ws, lr, eps, st);
-  return launch_reduce<TW, 8, 16>(t, K, V, scale, mean, grad, n, n_bags, L, ws, lr, eps, st);
+  bool v8 = ((uintptr_t)grad & 31) == 0;
+  for (const SlotInfo& si : t->sinfo_h) v8 = v8 && (si.dim % 8 == 0);
+  const int md = t->st.max_dim;
+#define EMB_RED(G, VW, NCB) return launch_reduce<TW, G, VW, NCB>(t, K, V, scale, mean, grad, n, n_bags, L, ws, lr, eps, st)
+  if (v8) {
+    if (md <= 8) EMB_RED(1, 8, 1);
+    if (md <= 16) EMB_RED(2, 8, 1);
+    if (md <= 32) EMB_RED(4, 8, 1);
+    if (md <= 64) EMB_RED(8, 8, 1);
+    if (md <= 128) EMB_RED(16, 8, 1);
+    if (md <= 256) EMB_RED(32, 8, 1);
+    EMB_RED(32, 8, 2);
+  }
+  if (md <= 4) EMB_RED(1, 4, 1);
+  if (md <= 8) EMB_RED(2, 4, 1);
+  if (md <= 16) EMB_RED(4, 4, 1);
+  if (md <= 32) EMB_RED(8, 4, 1);
+  if (md <= 64) EMB_RED(16, 4, 1);
+  if (md <= 128) EMB_RED(32, 4, 1);
+  if (md <= 256) EMB_RED(32, 4, 2);
+  EMB_RED(32, 4, 4);
+#undef EMB_RED
 }
 
 static int bits_for(unsigned x) {
@@ -705,6 +927,9 @@ static emb_status run_bwd(emb_table* table, const int64_t* offsets_d, int64_t n_
                           const WsLayout& L, cudaStream_t st) {
   const unsigned n = (unsigned)nnz;
   const unsigned miss = (unsigned)table->st.n_keys;
+  // grad_out rows are addressed as 32-bit float4 indices
+  if ((unsigned long long)(n_bags / table->st.n_slots) * (unsigned long long)table->st.sum_dims >= (1ULL << 34))
+    return fail(EMB_ERR_UNSUPPORTED, "grad_out larger than 2^34 elements");
   const int bits = bits_for(miss);  // rows and the miss sentinel fit in `bits`
   const int passes = std::max(1, (bits + kRadixBits - 1) / kRadixBits);
   const unsigned sorted_in_b = (unsigned)(passes & 1);
