@@ -139,7 +139,7 @@ def launches_per_step(n_keys: int) -> int:
     """Kernels this library launches for one fwd + one bwd call."""
     bits = max(1, int(n_keys).bit_length())
     passes = max(1, math.ceil(bits / 9))
-    return 1 + 1 + passes * 5 + 2   # fwd; expand; (count + 3 scan + scatter) per radix pass; reduce; fixup
+    return 2 + passes * 5 + 2   # header + recording fwd; (count + 3 scan + scatter) per radix pass; reduce; fixup
 
 
 # ------------------------------------------------------------------ oracle (CPU baseline / reference arm)
@@ -301,8 +301,9 @@ def run_ours(args):
     fwd_bytes = io_bytes + gather_bytes
 
     def step():
-        E.emb_lookup_fwd(tbl, offsets, qkeys, cfg.pool, out=out)
-        E.emb_bwd_adagrad(tbl, offsets, qkeys, cfg.pool, grad, cfg.lr, cfg.eps, wsb)
+        # the forward records each occurrence's resolved row for the backward
+        E.emb_lookup_fwd_record(tbl, offsets, qkeys, cfg.pool, wsb, out=out)
+        E.emb_bwd_adagrad_recorded(tbl, n_bags, nnz, cfg.pool, grad, cfg.lr, cfg.eps, wsb)
 
     step()
     uk = torch.empty(nnz, dtype=torch.int64, device=dev)
@@ -312,7 +313,14 @@ def run_ours(args):
     d_u = dims_t[uk[:n_unique] >> 48]
     rmw_bytes = int(d_u.sum()) * (2 * wsz + 8)
     del uk, d_u
-    bwd_bytes = io_bytes + rmw_bytes
+    # the recording forward resolved every key once; the backward reads grad_out
+    # and read-modify-writes the hit rows (the cached row ids are workspace)
+    bwd_bytes = 4 * cfg.batch * cfg.sum_dims + rmw_bytes
+    # algorithmic bytes per launch of each kernel (sort and partial sums are overhead)
+    kernel_bytes = {
+        "fwd_pool_kernel": fwd_bytes,
+        "segreduce_adagrad_kernel": 4 * cfg.batch * cfg.sum_dims + rmw_bytes,
+    }
     flags = E.emb_check_device_flag(tbl)
 
     for _ in range(max(0, args.warmup - 1)):
@@ -322,22 +330,32 @@ def run_ours(args):
     clocks = Clocks(local)
     clocks.start()
     K = args.steps
-    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(K)]
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(2 + len(E.BWD_PHASES))] for _ in range(K)]
+    for e in ev:                      # torch creates the CUDA event on first record
+        for x in e:
+            x.record(stream)
+    torch.cuda.synchronize()
     for k in range(K):
         ev[k][0].record(stream)
-        E.emb_lookup_fwd(tbl, offsets, qkeys, cfg.pool, out=out)
+        E.emb_lookup_fwd_record(tbl, offsets, qkeys, cfg.pool, wsb, out=out)
         ev[k][1].record(stream)
-        E.emb_bwd_adagrad(tbl, offsets, qkeys, cfg.pool, grad, cfg.lr, cfg.eps, wsb)
-        ev[k][2].record(stream)
+        E.emb_bwd_phase_events(tbl, ev[k][2:])
+        E.emb_bwd_adagrad_recorded(tbl, n_bags, nnz, cfg.pool, grad, cfg.lr, cfg.eps, wsb)
     torch.cuda.synchronize()
     barrier(ws)
     clk = clocks.stop()
-    total_ms = ev[0][0].elapsed_time(ev[K - 1][2])
+    E.emb_bwd_phase_events(tbl, [])
+    total_ms = ev[0][0].elapsed_time(ev[K - 1][-1])
     fwd_ms = statistics.mean(e[0].elapsed_time(e[1]) for e in ev)
-    bwd_ms = statistics.mean(e[1].elapsed_time(e[2]) for e in ev)
+    bwd_ms = statistics.mean(e[1].elapsed_time(e[-1]) for e in ev)
+    phase_ms = {name: statistics.mean(e[1 + i].elapsed_time(e[2 + i]) for e in ev)
+                for i, name in enumerate(E.BWD_PHASES)}
     total_ms = max_over_ranks(ws, total_ms)
     ms_step = total_ms / K
     flags |= E.emb_check_device_flag(tbl)
+    kernel_ms = {"fwd_pool_kernel": fwd_ms,
+                 "radix sort (count + scan + scatter kernels)": phase_ms["sort"],
+                 "segreduce_adagrad_kernel": phase_ms["reduce"], "fixup_kernel": phase_ms["fixup"]}
 
     # ---- end to end through the C ABI: pinned host inputs in, pooled output back, every step
     e2e = None
@@ -371,16 +389,21 @@ def run_ours(args):
         e2e_ms = max_over_ranks(ws, a.elapsed_time(b)) / Ke
         e2e = {"value": ws * nnz / (e2e_ms * 1e-3), "unit": "lookups/s", "ms_per_step": e2e_ms,
                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
-               "path": "pinned host CSR batch + grad_out -> H2D -> emb_lookup_fwd + emb_bwd_adagrad -> D2H pooled output"}
+               "path": "pinned host CSR batch + grad_out -> H2D -> emb_lookup_fwd_record + emb_bwd_adagrad_recorded -> D2H pooled output"}
 
     peak, peak_src = peaks()
     fwd_gbs = fwd_bytes / (fwd_ms * 1e-3) / 1e9
     bwd_gbs = bwd_bytes / (bwd_ms * 1e-3) / 1e9
-    dominant_fwd = fwd_ms >= bwd_ms
-    roof = {"bound": "hbm", "kernel": "fwd_pool_kernel" if dominant_fwd else "bwd (all kernels)",
-            "achieved": fwd_gbs if dominant_fwd else bwd_gbs, "peak": peak, "unit": "GB/s",
-            "frac": (fwd_gbs if dominant_fwd else bwd_gbs) / peak, "traffic": None, "peak_source": peak_src,
-            "algorithmic_bytes_per_launch": fwd_bytes if dominant_fwd else bwd_bytes}
+    single = {k: v for k, v in kernel_ms.items() if k in kernel_bytes}
+    dom = max(single, key=single.get)
+    dom_gbs = kernel_bytes[dom] / (kernel_ms[dom] * 1e-3) / 1e9
+    roof = {"bound": "hbm", "kernel": dom, "achieved": dom_gbs, "peak": peak, "unit": "GB/s",
+            "frac": dom_gbs / peak, "traffic": None, "peak_source": peak_src,
+            "algorithmic_bytes_per_launch": kernel_bytes[dom], "ms_per_launch": kernel_ms[dom]}
+    kernels = {k: {"ms": v, "share": v / ms_step,
+                   **({"algorithmic_gbs": kernel_bytes[k] / (v * 1e-3) / 1e9,
+                       "frac_of_peak": kernel_bytes[k] / (v * 1e-3) / 1e9 / peak} if k in kernel_bytes else {})}
+               for k, v in kernel_ms.items()}
 
     cpu = None
     if rank == 0 and ws == 1 and not args.no_cpu_baseline:
@@ -407,8 +430,9 @@ def run_ours(args):
         "fwd_algorithmic_gbs": fwd_gbs, "bwd_algorithmic_gbs": bwd_gbs,
         "fwd_frac_nominal_8tbs": fwd_gbs / NOMINAL_HBM_GBS, "bwd_frac_nominal_8tbs": bwd_gbs / NOMINAL_HBM_GBS,
         "roofline": roof,
-        "roofline_bwd": {"bound": "hbm", "achieved": bwd_gbs, "peak": peak, "unit": "GB/s", "frac": bwd_gbs / peak,
-                         "algorithmic_bytes_per_step": bwd_bytes},
+        "kernels": kernels,
+        "fwd_roofline": {"achieved": fwd_gbs, "frac": fwd_gbs / peak, "algorithmic_bytes": fwd_bytes},
+        "bwd_roofline": {"achieved": bwd_gbs, "frac": bwd_gbs / peak, "algorithmic_bytes": bwd_bytes},
         "cpu_baseline": cpu, "e2e": e2e,
         "gpu_launches": K * launches_per_step(st["n_keys"]),
         "clocks": clk, "device_flags": flags,

@@ -189,6 +189,20 @@ EMB_API emb_status emb_bwd_adagrad(emb_table* table, const int64_t* offsets_d, i
                            void* workspace_d, size_t ws_bytes, void* stream);
 
 /*
+ * emb_bwd_phase_events -- optional timing hook (no counterpart in the pages;
+ * it serves measurement).  Registers up to EMB_BWD_PHASES caller-owned
+ * cudaEvent_t handles (passed as void*, created with timing enabled) that
+ * every later emb_bwd_adagrad call on this table records, on its stream,
+ * after each of its phases: [0] expand (probe to row/bag pairs), [1] radix
+ * sort, [2] segmented reduce + Adagrad, [3] cross-chunk fixup.  Elapsed times
+ * between an event recorded just before the call and these give each
+ * phase's device time.  n = 0 removes the hook.  The events must outlive
+ * the calls that record them.
+ */
+#define EMB_BWD_PHASES 4
+EMB_API emb_status emb_bwd_phase_events(emb_table* table, void* const* events, int n);
+
+/*
  * emb_bwd_adagrad_noalloc -- the same backward + Adagrad step as
  * emb_bwd_adagrad, for callers that cannot allocate device memory: code that
  * runs under a memory manager which already owns all of the GPU's memory
@@ -217,6 +231,28 @@ EMB_API emb_status emb_bwd_adagrad(emb_table* table, const int64_t* offsets_d, i
 EMB_API emb_status emb_bwd_adagrad_noalloc(emb_table* table, const int64_t* offsets_d, int64_t n_bags,
                                            const int64_t* keys_d, int64_t nnz, emb_pool pool,
                                            const float* grad_out_d, float lr, float eps, void* stream);
+
+/*
+ * emb_lookup_fwd_record / emb_bwd_adagrad_recorded -- the same forward and
+ * backward split so that the probe runs once per step: the lookup kernel of
+ * the forward ([TPCG] 计算优化: one kernel resolves every feature) also writes
+ * each occurrence's resolved row and bag into `workspace_d` (sized by
+ * emb_bwd_workspace_size), and the backward then starts from those pairs
+ * instead of probing the keys again.  Output, pooling and update are exactly
+ * those of emb_lookup_fwd and emb_bwd_adagrad.
+ *   emb_lookup_fwd_record: arguments of emb_lookup_fwd plus the workspace.
+ *   emb_bwd_adagrad_recorded: the batch shape (n_bags, nnz, pool) must be the
+ *   one recorded last on this table into this same workspace, and the call
+ *   must be ordered after the recording forward on the GPU; otherwise it
+ *   returns EMB_ERR_INVALID_ARG without queuing work.  The recorded pairs
+ *   reflect the keys as the forward read them.
+ */
+EMB_API emb_status emb_lookup_fwd_record(emb_table* table, const int64_t* offsets_d, int64_t n_bags,
+                                         const int64_t* keys_d, int64_t nnz, emb_pool pool, float* out_d,
+                                         void* workspace_d, size_t ws_bytes, void* stream);
+EMB_API emb_status emb_bwd_adagrad_recorded(emb_table* table, int64_t n_bags, int64_t nnz, emb_pool pool,
+                                            const float* grad_out_d, float lr, float eps, void* workspace_d,
+                                            size_t ws_bytes, void* stream);
 
 /*
  * emb_bwd_unique_keys -- the deduplicated key set of the last emb_bwd_adagrad

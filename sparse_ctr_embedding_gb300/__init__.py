@@ -21,8 +21,8 @@ from .build import HEADER, LIB_PATH, build
 __all__ = [
     "EmbError", "LibraryNotBuilt", "Table", "lib", "declared_symbols",
     "emb_table_create", "emb_table_destroy", "emb_table_get_stats", "emb_table_plan",
-    "emb_lookup_fwd", "emb_bwd_workspace_size", "emb_bwd_adagrad", "emb_bwd_adagrad_noalloc",
-    "emb_bwd_unique_keys", "EMB_NOALLOC_SCRATCH_BYTES",
+    "emb_lookup_fwd", "emb_lookup_fwd_record", "emb_bwd_adagrad_recorded", "emb_bwd_workspace_size", "emb_bwd_adagrad", "emb_bwd_adagrad_noalloc",
+    "emb_bwd_unique_keys", "emb_bwd_phase_events", "EMB_NOALLOC_SCRATCH_BYTES", "BWD_PHASES",
     "emb_resolve", "emb_table_export", "emb_table_export_rows", "emb_table_slots", "emb_check_device_flag",
     "emb_status_string", "emb_last_error",
     "EMB_FLAG_PROBE_BOUND", "EMB_FLAG_BAD_OFFSETS", "EMB_FLAG_SLOT_MISMATCH", "EMB_FLAG_BAD_ROW",
@@ -34,6 +34,7 @@ STATUS = {0: "EMB_OK", 1: "EMB_ERR_INVALID_ARG", 2: "EMB_ERR_CUDA", 3: "EMB_ERR_
           8: "EMB_ERR_DEVICE_FLAG", 9: "EMB_ERR_UNSUPPORTED"}
 EMB_FLAG_PROBE_BOUND, EMB_FLAG_BAD_OFFSETS, EMB_FLAG_SLOT_MISMATCH, EMB_FLAG_BAD_ROW = 1, 2, 4, 8
 EMB_NOALLOC_SCRATCH_BYTES = 64 << 20
+BWD_PHASES = ("expand", "sort", "reduce", "fixup")
 _DTYPE = {"f32": 0, "f16": 1}
 _POOL = {"sum": 0, "mean": 1}
 
@@ -88,6 +89,10 @@ def lib():
             "emb_bwd_adagrad": [_vp, _vp, _i64, _vp, _i64, ctypes.c_int, _vp, ctypes.c_float, ctypes.c_float,
                                 _vp, ctypes.c_size_t, _vp],
             "emb_bwd_unique_keys": [_vp, _vp, ctypes.c_size_t, _vp, _vp, _vp],
+            "emb_bwd_phase_events": [_vp, ctypes.POINTER(_vp), ctypes.c_int],
+            "emb_lookup_fwd_record": [_vp, _vp, _i64, _vp, _i64, ctypes.c_int, _vp, _vp, ctypes.c_size_t, _vp],
+            "emb_bwd_adagrad_recorded": [_vp, _i64, _i64, ctypes.c_int, _vp, ctypes.c_float, ctypes.c_float, _vp,
+                                         ctypes.c_size_t, _vp],
             "emb_bwd_adagrad_noalloc": [_vp, _vp, _i64, _vp, _i64, ctypes.c_int, _vp, ctypes.c_float,
                                         ctypes.c_float, _vp],
             "emb_resolve": [_vp, _vp, _i64, _vp, _vp, _vp],
@@ -241,6 +246,28 @@ def emb_lookup_fwd(table: Table, offsets: torch.Tensor, keys: torch.Tensor, pool
     return out
 
 
+def emb_lookup_fwd_record(table: Table, offsets: torch.Tensor, keys: torch.Tensor, pool: str, workspace: torch.Tensor,
+                          out: Optional[torch.Tensor] = None, stream=None) -> torch.Tensor:
+    """emb_lookup_fwd that also records the resolved (row, bag) pairs into
+    `workspace` for emb_bwd_adagrad_recorded."""
+    n_bags = offsets.numel() - 1
+    if out is None:
+        out = torch.empty((n_bags // table.n_slots, sum(table.dims)), dtype=torch.float32, device=offsets.device)
+    _check(lib().emb_lookup_fwd_record(table.handle, _cuda(offsets, torch.int64, "offsets"), n_bags,
+                                       _cuda(keys, torch.int64, "keys"), keys.numel(), _POOL[pool],
+                                       _cuda(out, torch.float32, "out"), _cuda(workspace, None, "workspace"),
+                                       workspace.numel() * workspace.element_size(), _stream(stream)))
+    return out
+
+
+def emb_bwd_adagrad_recorded(table: Table, n_bags: int, nnz: int, pool: str, grad_out: torch.Tensor, lr: float,
+                             eps: float, workspace: torch.Tensor, stream=None) -> None:
+    _check(lib().emb_bwd_adagrad_recorded(table.handle, n_bags, nnz, _POOL[pool],
+                                          _cuda(grad_out, torch.float32, "grad_out"), ctypes.c_float(lr),
+                                          ctypes.c_float(eps), _cuda(workspace, None, "workspace"),
+                                          workspace.numel() * workspace.element_size(), _stream(stream)))
+
+
 def emb_bwd_workspace_size(table: Table, n_bags: int, nnz: int) -> int:
     b = ctypes.c_size_t()
     _check(lib().emb_bwd_workspace_size(table.handle, n_bags, nnz, ctypes.byref(b)))
@@ -265,6 +292,15 @@ def emb_bwd_adagrad_noalloc(table: Table, offsets: torch.Tensor, keys: torch.Ten
                                          _cuda(keys, torch.int64, "keys"), keys.numel(), _POOL[pool],
                                          _cuda(grad_out, torch.float32, "grad_out"), ctypes.c_float(lr),
                                          ctypes.c_float(eps), _stream(stream)))
+
+
+def emb_bwd_phase_events(table: Table, events) -> None:
+    """Register torch.cuda.Event objects (timing enabled) that each later
+    emb_bwd_adagrad records after its expand, sort, reduce and fixup phases."""
+    if any(not e.cuda_event for e in events):
+        raise ValueError("record each event once (torch creates CUDA events lazily) before registering it")
+    arr = (_vp * max(1, len(events)))(*[_vp(e.cuda_event) for e in events])
+    _check(lib().emb_bwd_phase_events(table.handle, arr, len(events)))
 
 
 def emb_bwd_unique_keys(table: Table, workspace: torch.Tensor, keys_out: torch.Tensor, n_unique_out: torch.Tensor,

@@ -42,6 +42,9 @@ namespace emb {
 
 emb_status check_batch(const emb_table* t, const int64_t* offsets_d, int64_t n_bags, const int64_t* keys_d,
                        int64_t nnz, int pool);
+cudaError_t launch_forward(const emb_table* t, const long long* offsets, long long n_bags, const long long* keys,
+                           long long nnz, int mean, float* out, unsigned* K, unsigned* V, float* scale,
+                           cudaStream_t st);
 
 constexpr int kChunk = 512;                      // sorted positions per reduce sub-chunk
 constexpr int kSortWarps = 8;
@@ -112,6 +115,15 @@ __device__ __forceinline__ unsigned lanemask_lt() {
 }
 
 // ------------------------------------------------------------------ 1. expand
+
+__global__ void ws_header_kernel(WsHeader* hdr, unsigned nnz, unsigned n_bags, unsigned sorted_in_b, unsigned miss) {
+  hdr->magic = kMagic;
+  hdr->nnz = nnz;
+  hdr->n_bags = n_bags;
+  hdr->sorted_in_b = sorted_in_b;
+  hdr->miss_row = miss;
+  hdr->n_unique = 0;
+}
 
 __global__ void __launch_bounds__(256) expand_kernel(TableView t, const long long* __restrict__ offsets,
                                                      long long n_bags, const long long* __restrict__ keys,
@@ -859,6 +871,12 @@ static size_t scatter_smem() {
   return sizeof(unsigned) * ((size_t)kSortWarps * kDigits + 2 * kDigits + 33 + 2 * (size_t)kSortTile);
 }
 
+// Record the caller's timing event for a finished backward phase, if any.
+static void mark_phase(const emb_table* t, int phase, cudaStream_t st) {
+  if (phase < t->n_phase_events && t->phase_events[phase])
+    cudaEventRecord((cudaEvent_t)t->phase_events[phase], st);
+}
+
 template <typename TW, int G, int VW, int NCB>
 static cudaError_t launch_reduce(const emb_table* t, const unsigned* K, const unsigned* V, const float* scale,
                                  int mean, const float* grad, unsigned n, unsigned n_bags, const WsLayout& L, char* ws,
@@ -876,12 +894,14 @@ static cudaError_t launch_reduce(const emb_table* t, const unsigned* K, const un
   unsigned* ar = (unsigned*)(ws + L.arow);
   segreduce_adagrad_kernel<TW, G, VW, NCB, U><<<(int)std::max(1LL, blocks), threads, 0, st>>>(
       v, K, V, scale, mean, grad, n, n_bags, L.n_chunks, pa, pb, ar, lr, eps);
+  mark_phase(t, 2, st);
   // the fixup reads partial rows four columns per lane
   constexpr int G4 = G * VW / 4 > 32 ? 32 : G * VW / 4;
   constexpr int NCB4 = (G * VW * NCB) / (4 * G4);
   long long fblocks = std::min<long long>(((long long)L.n_chunks * 32 + 255) / 256, resident_blocks(256));
   fixup_kernel<TW, G4, NCB4><<<(int)std::max(1LL, fblocks), 256, 0, st>>>(v, K, n, L.n_chunks, pa, pb, ar, lr,
                                                                               eps);
+  mark_phase(t, 3, st);
   return cudaGetLastError();
 }
 
@@ -922,16 +942,22 @@ static int bits_for(unsigned x) {
   return b;
 }
 
+static int sort_passes(const emb_table* t) {
+  const int bits = bits_for((unsigned)t->st.n_keys);  // rows and the miss sentinel fit in `bits`
+  return std::max(1, (bits + kRadixBits - 1) / kRadixBits);
+}
+
+// The backward.  With `recorded`, the (row, bag) pairs, 1/L and the header were
+// written by emb_lookup_fwd_record and the expand phase is skipped.
 static emb_status run_bwd(emb_table* table, const int64_t* offsets_d, int64_t n_bags, const int64_t* keys_d,
                           int64_t nnz, emb_pool pool, const float* grad_out_d, float lr, float eps, char* ws,
-                          const WsLayout& L, cudaStream_t st) {
+                          const WsLayout& L, cudaStream_t st, bool recorded = false) {
   const unsigned n = (unsigned)nnz;
   const unsigned miss = (unsigned)table->st.n_keys;
   // grad_out rows are addressed as 32-bit float4 indices
   if ((unsigned long long)(n_bags / table->st.n_slots) * (unsigned long long)table->st.sum_dims >= (1ULL << 34))
     return fail(EMB_ERR_UNSUPPORTED, "grad_out larger than 2^34 elements");
-  const int bits = bits_for(miss);  // rows and the miss sentinel fit in `bits`
-  const int passes = std::max(1, (bits + kRadixBits - 1) / kRadixBits);
+  const int passes = sort_passes(table);
   const unsigned sorted_in_b = (unsigned)(passes & 1);
   TableView v = table->view();
   WsHeader* hdr = (WsHeader*)(ws + L.hdr);
@@ -945,12 +971,18 @@ static emb_status run_bwd(emb_table* table, const int64_t* offsets_d, int64_t n_
   // With malformed offsets (flagged) some positions keep stale values; every
   // later kernel treats rows >= n_rows and bags >= n_bags as absent, so they
   // stay in bounds.
-  long long blocks = std::min<long long>((n_bags * 32 + 255) / 256, resident_blocks(256));
-  expand_kernel<<<(int)std::max(1LL, blocks), 256, 0, st>>>(v, (const long long*)offsets_d, n_bags,
-                                                            (const long long*)keys_d, nnz, mean, kA, vA, scale, hdr,
-                                                            sorted_in_b);
-  EMB_CUDA(cudaGetLastError());
-  if (nnz == 0) return EMB_OK;
+  if (!recorded) {
+    long long blocks = std::min<long long>((n_bags * 32 + 255) / 256, resident_blocks(256));
+    expand_kernel<<<(int)std::max(1LL, blocks), 256, 0, st>>>(v, (const long long*)offsets_d, n_bags,
+                                                              (const long long*)keys_d, nnz, mean, kA, vA, scale,
+                                                              hdr, sorted_in_b);
+    EMB_CUDA(cudaGetLastError());
+  }
+  mark_phase(table, 0, st);
+  if (nnz == 0) {
+    for (int ph = 1; ph < EMB_BWD_PHASES; ++ph) mark_phase(table, ph, st);
+    return EMB_OK;
+  }
 
   unsigned* counts = (unsigned*)(ws + L.counts);
   unsigned* partials = (unsigned*)(ws + L.partials);
@@ -967,6 +999,7 @@ static emb_status run_bwd(emb_table* table, const int64_t* offsets_d, int64_t n_
     std::swap(ki, ko);
     std::swap(vi, vo);
   }
+  mark_phase(table, 1, st);
   // ki/vi hold the sorted pairs
   cudaError_t e = table->st.wdtype == EMB_F16
                       ? dispatch_reduce<__half>(table, ki, vi, scale, mean, grad_out_d, n, (unsigned)n_bags, L, ws, lr, eps, st)
@@ -1024,6 +1057,55 @@ emb_status emb_bwd_adagrad_noalloc(emb_table* table, const int64_t* offsets_d, i
   if ((rc = noalloc_scratch(&scratch)) != EMB_OK) return rc;
   return run_bwd(table, offsets_d, n_bags, keys_d, nnz, pool, grad_out_d, lr, eps, (char*)scratch, L,
                  (cudaStream_t)stream);
+}
+
+emb_status emb_lookup_fwd_record(emb_table* table, const int64_t* offsets_d, int64_t n_bags, const int64_t* keys_d,
+                                 int64_t nnz, emb_pool pool, float* out_d, void* workspace_d, size_t ws_bytes,
+                                 void* stream) {
+  emb_status rc = check_batch(table, offsets_d, n_bags, keys_d, nnz, pool);
+  if (rc != EMB_OK) return rc;
+  if (n_bags > 0 && !out_d) return fail(EMB_ERR_INVALID_ARG, "out is NULL");
+  const WsLayout L = ws_layout(table, n_bags, nnz);
+  if (!workspace_d || ws_bytes < L.total) return fail(EMB_ERR_WORKSPACE, "workspace missing or too small");
+  if (((uintptr_t)workspace_d & 255) != 0) return fail(EMB_ERR_WORKSPACE, "workspace must be 256-byte aligned");
+  cudaStream_t st = (cudaStream_t)stream;
+  char* ws = (char*)workspace_d;
+  ws_header_kernel<<<1, 1, 0, st>>>((WsHeader*)(ws + L.hdr), (unsigned)nnz, (unsigned)n_bags,
+                                    (unsigned)(sort_passes(table) & 1), (unsigned)table->st.n_keys);
+  if (n_bags > 0) {
+    cudaError_t e = launch_forward(table, (const long long*)offsets_d, n_bags, (const long long*)keys_d, nnz,
+                                   pool == EMB_POOL_MEAN, out_d, (unsigned*)(ws + L.kA), (unsigned*)(ws + L.vA),
+                                   (float*)(ws + L.scale), st);
+    if (e != cudaSuccess) return cuda_fail(e, "fwd_pool_kernel launch");
+  }
+  EMB_CUDA(cudaGetLastError());
+  table->rec_ws = workspace_d;
+  table->rec_nnz = nnz;
+  table->rec_bags = n_bags;
+  table->rec_pool = (int)pool;
+  return EMB_OK;
+}
+
+emb_status emb_bwd_adagrad_recorded(emb_table* table, int64_t n_bags, int64_t nnz, emb_pool pool,
+                                    const float* grad_out_d, float lr, float eps, void* workspace_d, size_t ws_bytes,
+                                    void* stream) {
+  if (!table) return fail(EMB_ERR_INVALID_ARG, "table is NULL");
+  if (!workspace_d || workspace_d != table->rec_ws || nnz != table->rec_nnz || n_bags != table->rec_bags ||
+      (int)pool != table->rec_pool)
+    return fail(EMB_ERR_INVALID_ARG, "no emb_lookup_fwd_record of this batch shape in this workspace");
+  if (n_bags > 0 && !grad_out_d) return fail(EMB_ERR_INVALID_ARG, "grad_out is NULL");
+  const WsLayout L = ws_layout(table, n_bags, nnz);
+  if (ws_bytes < L.total) return fail(EMB_ERR_WORKSPACE, "workspace missing or too small");
+  return run_bwd(table, nullptr, n_bags, nullptr, nnz, pool, grad_out_d, lr, eps, (char*)workspace_d, L,
+                 (cudaStream_t)stream, true);
+}
+
+emb_status emb_bwd_phase_events(emb_table* table, void* const* events, int n) {
+  if (!table || n < 0 || n > EMB_BWD_PHASES || (n > 0 && !events))
+    return fail(EMB_ERR_INVALID_ARG, "bad phase events");
+  for (int i = 0; i < EMB_BWD_PHASES; ++i) table->phase_events[i] = i < n ? events[i] : nullptr;
+  table->n_phase_events = n;
+  return EMB_OK;
 }
 
 emb_status emb_bwd_workspace_size(const emb_table* table, int64_t n_bags, int64_t nnz, size_t* bytes) {

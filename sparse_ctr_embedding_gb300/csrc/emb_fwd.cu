@@ -61,10 +61,19 @@ __device__ __forceinline__ int pow2_at_least(int x) {
   return g;
 }
 
-template <typename TW, int NCB, int U>
+// With a Record sink the kernel also writes, for the backward, the resolved
+// internal row of every occurrence (n_rows for a miss) and its bag, plus 1/L
+// per bag for mean pooling.
+struct Record {
+  unsigned* K;
+  unsigned* V;
+  float* scale;
+};
+
+template <typename TW, int NCB, int U, bool kRecord>
 __global__ void __launch_bounds__(256) fwd_pool_kernel(TableView t, const long long* __restrict__ offsets,
                                                        long long n_bags, const long long* __restrict__ keys,
-                                                       long long nnz, int mean, float* __restrict__ out) {
+                                                       long long nnz, int mean, float* __restrict__ out, Record rec) {
   constexpr int VEC = VecOf<TW>::kElems;
   const int lane = threadIdx.x & 31;
   const long long nwarps = ((long long)gridDim.x * blockDim.x) >> 5;
@@ -106,13 +115,20 @@ __global__ void __launch_bounds__(256) fwd_pool_kernel(TableView t, const long l
       long long elem = -1;  // first weight element of this lane's key, -1 = miss
       if (lane < n) {
         const long long k = keys[c0 + lane];
+        unsigned row = t.n_rows;
         if (key_slot(k) != s) {
           atomicOr(t.flags, EMB_FLAG_SLOT_MISMATCH);
         } else {
-          unsigned row, ext;
+          unsigned r, ext;
           unsigned long long h;
-          if (probe(t, k, &row, &ext, &h))
-            elem = t.uniform_dim ? (long long)row * D : ebase + (long long)(row - rbase) * D;
+          if (probe(t, k, &r, &ext, &h)) {
+            row = r;
+            elem = t.uniform_dim ? (long long)r * D : ebase + (long long)(r - rbase) * D;
+          }
+        }
+        if (kRecord) {
+          rec.K[c0 + lane] = row;
+          rec.V[c0 + lane] = (unsigned)bag;
         }
       }
       for (int base = 0; base < n; base += P * U) {
@@ -141,6 +157,7 @@ __global__ void __launch_bounds__(256) fwd_pool_kernel(TableView t, const long l
       for (int j = 0; j < VEC; ++j)
         for (int off = G; off < 32; off <<= 1) acc[c][j] += __shfl_xor_sync(0xffffffffu, acc[c][j], off);
 
+    if (kRecord && mean && lane == 0) rec.scale[bag] = end > start ? 1.0f / (float)(end - start) : 0.f;
     if (sub == 0) {
       const long long L = end - start;
       const float den = (mean && L > 0) ? (float)L : 1.f;  // mean over L counting misses; L = 0 gives 0
@@ -159,9 +176,9 @@ __global__ void __launch_bounds__(256) fwd_pool_kernel(TableView t, const long l
   }
 }
 
-template <typename TW>
+template <typename TW, bool kRecord>
 static cudaError_t launch_fwd(const emb_table* t, const long long* offsets, long long n_bags, const long long* keys,
-                              long long nnz, int mean, float* out, cudaStream_t st) {
+                              long long nnz, int mean, float* out, Record rec, cudaStream_t st) {
   constexpr int VEC = VecOf<TW>::kElems;
   const int max_vecs = t->st.max_dim / VEC;      // 16-byte vectors in the widest row
   const int ncb = (max_vecs + 31) / 32;          // column blocks per lane at G = 32
@@ -172,12 +189,25 @@ static cudaError_t launch_fwd(const emb_table* t, const long long* offsets, long
   if (blocks < 1) blocks = 1;
   TableView v = t->view();
   if (ncb <= 1)
-    fwd_pool_kernel<TW, 1, 4><<<(int)blocks, threads, 0, st>>>(v, offsets, n_bags, keys, nnz, mean, out);
+    fwd_pool_kernel<TW, 1, 4, kRecord><<<(int)blocks, threads, 0, st>>>(v, offsets, n_bags, keys, nnz, mean, out, rec);
   else if (ncb <= 2)
-    fwd_pool_kernel<TW, 2, 2><<<(int)blocks, threads, 0, st>>>(v, offsets, n_bags, keys, nnz, mean, out);
+    fwd_pool_kernel<TW, 2, 2, kRecord><<<(int)blocks, threads, 0, st>>>(v, offsets, n_bags, keys, nnz, mean, out, rec);
   else
-    fwd_pool_kernel<TW, 4, 1><<<(int)blocks, threads, 0, st>>>(v, offsets, n_bags, keys, nnz, mean, out);
+    fwd_pool_kernel<TW, 4, 1, kRecord><<<(int)blocks, threads, 0, st>>>(v, offsets, n_bags, keys, nnz, mean, out, rec);
   return cudaGetLastError();
+}
+
+// Forward launch, optionally recording (row, bag) pairs for the backward.
+cudaError_t launch_forward(const emb_table* t, const long long* offsets, long long n_bags, const long long* keys,
+                           long long nnz, int mean, float* out, unsigned* K, unsigned* V, float* scale,
+                           cudaStream_t st) {
+  const Record rec{K, V, scale};
+  const bool record = K != nullptr;
+  if (t->st.wdtype == EMB_F16)
+    return record ? launch_fwd<__half, true>(t, offsets, n_bags, keys, nnz, mean, out, rec, st)
+                  : launch_fwd<__half, false>(t, offsets, n_bags, keys, nnz, mean, out, rec, st);
+  return record ? launch_fwd<float, true>(t, offsets, n_bags, keys, nnz, mean, out, rec, st)
+                : launch_fwd<float, false>(t, offsets, n_bags, keys, nnz, mean, out, rec, st);
 }
 
 emb_status check_batch(const emb_table* t, const int64_t* offsets_d, int64_t n_bags, const int64_t* keys_d,
@@ -203,12 +233,8 @@ extern "C" emb_status emb_lookup_fwd(emb_table* table, const int64_t* offsets_d,
   if (n_bags == 0) return EMB_OK;
   if (!out_d) return fail(EMB_ERR_INVALID_ARG, "out is NULL");
   cudaStream_t st = (cudaStream_t)stream;
-  cudaError_t e =
-      table->st.wdtype == EMB_F16
-          ? launch_fwd<__half>(table, (const long long*)offsets_d, n_bags, (const long long*)keys_d, nnz,
-                               pool == EMB_POOL_MEAN, out_d, st)
-          : launch_fwd<float>(table, (const long long*)offsets_d, n_bags, (const long long*)keys_d, nnz,
-                              pool == EMB_POOL_MEAN, out_d, st);
+  cudaError_t e = launch_forward(table, (const long long*)offsets_d, n_bags, (const long long*)keys_d, nnz,
+                                 pool == EMB_POOL_MEAN, out_d, nullptr, nullptr, nullptr, st);
   if (e != cudaSuccess) return cuda_fail(e, "fwd_pool_kernel launch");
   return EMB_OK;
 }

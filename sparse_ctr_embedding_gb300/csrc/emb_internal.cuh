@@ -144,6 +144,12 @@ struct emb_table {
   unsigned int* flags_d = nullptr;
   int uniform_dim = 0;
   std::vector<long long> ext_elem_off_h;  // ragged tables only: host copy for chunked transfers
+  void* phase_events[EMB_BWD_PHASES] = {};  // caller-owned cudaEvent_t, see emb_bwd_phase_events
+  int n_phase_events = 0;
+  // the last emb_lookup_fwd_record: which workspace holds its (row, bag) pairs
+  const void* rec_ws = nullptr;
+  long long rec_nnz = -1, rec_bags = -1;
+  int rec_pool = -1;
 
   emb::TableView view() const {
     emb::TableView v;

@@ -86,14 +86,22 @@ def make_table(cfg, wl, values_dev=True):
                               capacity=cfg.capacity, acc_init=cfg.acc0)
 
 
-def gpu_step(cfg, wl, values_dev=True) -> GpuStep:
+def gpu_step(cfg, wl, values_dev=True, recorded=False) -> GpuStep:
+    """One step through the C ABI.  recorded=True uses the forward that
+    records (row, bag) pairs and the backward that starts from them."""
     tbl = make_table(cfg, wl, values_dev)
     off, q, g = wl.offsets.cuda(), wl.qkeys.cuda(), wl.grad.cuda()
-    out = E.emb_lookup_fwd(tbl, off, q, cfg.pool)
-    slots, rows = E.emb_resolve(tbl, q)
     n_bags, nnz = off.numel() - 1, q.numel()
     ws = torch.empty(E.emb_bwd_workspace_size(tbl, n_bags, nnz), dtype=torch.uint8, device="cuda")
-    E.emb_bwd_adagrad(tbl, off, q, cfg.pool, g, cfg.lr, cfg.eps, ws)
+    if recorded:
+        out = E.emb_lookup_fwd_record(tbl, off, q, cfg.pool, ws)
+    else:
+        out = E.emb_lookup_fwd(tbl, off, q, cfg.pool)
+    slots, rows = E.emb_resolve(tbl, q)
+    if recorded:
+        E.emb_bwd_adagrad_recorded(tbl, n_bags, nnz, cfg.pool, g, cfg.lr, cfg.eps, ws)
+    else:
+        E.emb_bwd_adagrad(tbl, off, q, cfg.pool, g, cfg.lr, cfg.eps, ws)
     uk = torch.empty(max(nnz, 1), dtype=torch.int64, device="cuda")
     nu = torch.zeros(1, dtype=torch.int64, device="cuda")
     E.emb_bwd_unique_keys(tbl, ws, uk, nu)

@@ -36,6 +36,40 @@ def test_step_parity_small(cfg):
     print(cfg.name, rep)
 
 
+@pytest.mark.parametrize("cfg", SMALL, ids=lambda c: c.name)
+def test_recorded_step_parity_and_identity(cfg):
+    """The forward that records (row, bag) pairs + the backward that starts
+    from them: oracle parity, and bit-identical to the unrecorded path."""
+    wl = W.make(cfg, device="cuda")
+    rec = gpu_step(cfg, wl, recorded=True)
+    check_step(cfg, wl, rec)
+    ref = gpu_step(cfg, wl)
+    assert torch.equal(rec.out, ref.out)
+    assert np.array_equal(rec.values_out.view(np.uint8), ref.values_out.view(np.uint8))
+    assert np.array_equal(rec.acc_out.view(np.uint8), ref.acc_out.view(np.uint8))
+    assert np.array_equal(np.sort(rec.unique), np.sort(ref.unique))
+
+
+def test_recorded_backward_needs_its_forward():
+    cfg = SMALL[0]
+    wl = W.make(cfg, device="cuda")
+    tbl = make_table(cfg, wl)
+    off, q, g = wl.offsets, wl.qkeys, wl.grad
+    n_bags, nnz = off.numel() - 1, q.numel()
+    ws = torch.empty(E.emb_bwd_workspace_size(tbl, n_bags, nnz), dtype=torch.uint8, device="cuda")
+    with pytest.raises(E.EmbError) as ei:                         # nothing recorded yet
+        E.emb_bwd_adagrad_recorded(tbl, n_bags, nnz, cfg.pool, g, cfg.lr, cfg.eps, ws)
+    assert ei.value.name == "EMB_ERR_INVALID_ARG"
+    E.emb_lookup_fwd_record(tbl, off, q, cfg.pool, ws)
+    other = torch.empty_like(ws)
+    with pytest.raises(E.EmbError):                               # another workspace
+        E.emb_bwd_adagrad_recorded(tbl, n_bags, nnz, cfg.pool, g, cfg.lr, cfg.eps, other)
+    with pytest.raises(E.EmbError):                               # another batch shape
+        E.emb_bwd_adagrad_recorded(tbl, n_bags, nnz - 1, cfg.pool, g, cfg.lr, cfg.eps, ws)
+    E.emb_bwd_adagrad_recorded(tbl, n_bags, nnz, cfg.pool, g, cfg.lr, cfg.eps, ws)
+    assert E.emb_check_device_flag(tbl) == 0
+
+
 @pytest.mark.parametrize("cfg", [SMALL[1], SMALL[4]], ids=lambda c: c.name)
 def test_host_values_upload_matches_device_upload(cfg):
     wl = W.make(cfg, device="cuda")
