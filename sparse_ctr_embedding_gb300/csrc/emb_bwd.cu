@@ -168,17 +168,24 @@ __global__ void __launch_bounds__(256) expand_kernel(TableView t, const long lon
 
 // ------------------------------------------------------------------ 2. radix sort
 
-// Per-warp digit counting over one tile: each warp walks its 32*kSortItems
+// Stable per-warp ranking over one tile: each warp walks its 32*kSortItems
 // consecutive keys in order, 32 at a time; lanes holding the same digit are
-// grouped with __match_any_sync and the group leader bumps the warp's counter.
-// Returns, per item, its rank among equal digits of this warp (stable).
+// found with one ballot per digit bit, and the group leader bumps the warp's
+// counter.  Returns, per item, its rank among equal digits of this warp.
 __device__ __forceinline__ void warp_rank(unsigned (&d)[kSortItems], unsigned (&rank)[kSortItems], bool (&valid)[kSortItems],
                                           unsigned* cnt /* this warp's kDigits counters */) {
   const int lane = threadIdx.x & 31;
 #pragma unroll
   for (int r = 0; r < kSortItems; ++r) {
-    const unsigned key = valid[r] ? d[r] : 0xFFFFFFFFu;
-    const unsigned peers = __match_any_sync(0xffffffffu, key);
+    // lanes holding the same digit: one ballot per digit bit, plus validity
+    const unsigned vb = __ballot_sync(0xffffffffu, valid[r]);
+    unsigned peers = valid[r] ? vb : ~vb;
+#pragma unroll
+    for (int b = 0; b < kRadixBits; ++b) {
+      const unsigned bit = (d[r] >> b) & 1u;
+      const unsigned bb = __ballot_sync(0xffffffffu, bit);
+      peers &= bit ? bb : ~bb;
+    }
     const int leader = __ffs(peers) - 1;
     unsigned base = 0;
     if (valid[r] && lane == leader) {
@@ -191,24 +198,45 @@ __device__ __forceinline__ void warp_rank(unsigned (&d)[kSortItems], unsigned (&
   }
 }
 
+// Digit counts of one tile (the same kSortTile keys the scatter kernel ranks).
+// Each thread takes kSortItems consecutive keys and adds whole runs of equal
+// digits with one shared atomic (sorted passes and hot rows give long runs).
 __global__ void __launch_bounds__(kSortThreads) radix_count_kernel(const unsigned* __restrict__ keys, unsigned n,
                                                                    int shift, unsigned* __restrict__ counts,
                                                                    unsigned n_tiles) {
   __shared__ unsigned cnt[kSortWarps][kDigits];
-  const int w = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int w = threadIdx.x >> 5;
   for (int i = threadIdx.x; i < kSortWarps * kDigits; i += kSortThreads) (&cnt[0][0])[i] = 0;
   __syncthreads();
   const unsigned tile = blockIdx.x;
-  const unsigned base = tile * kSortTile + w * 32 * kSortItems;
-  unsigned d[kSortItems], rank[kSortItems];
-  bool valid[kSortItems];
+  const unsigned base = tile * kSortTile + threadIdx.x * kSortItems;
+  unsigned k[kSortItems];
+  if (base + kSortItems <= n) {
+    const uint4* p = reinterpret_cast<const uint4*>(keys + base);
 #pragma unroll
-  for (int r = 0; r < kSortItems; ++r) {
-    const unsigned i = base + r * 32 + lane;
-    valid[r] = i < n;
-    d[r] = valid[r] ? (keys[i] >> shift) & (kDigits - 1) : 0;
+    for (int q = 0; q < kSortItems / 4; ++q) {
+      const uint4 x = __ldg(p + q);
+      k[4 * q] = x.x; k[4 * q + 1] = x.y; k[4 * q + 2] = x.z; k[4 * q + 3] = x.w;
+    }
+  } else {
+#pragma unroll
+    for (int j = 0; j < kSortItems; ++j) k[j] = base + j < n ? keys[base + j] : 0u;
   }
-  warp_rank(d, rank, valid, cnt[w]);
+  const int m = base >= n ? 0 : (int)min((unsigned)kSortItems, n - base);
+  unsigned cur = 0, run = 0;
+#pragma unroll
+  for (int j = 0; j < kSortItems; ++j) {
+    if (j < m) {
+      const unsigned dg = (k[j] >> shift) & (kDigits - 1);
+      if (run && dg != cur) {
+        atomicAdd(&cnt[w][cur], run);
+        run = 0;
+      }
+      cur = dg;
+      ++run;
+    }
+  }
+  if (run) atomicAdd(&cnt[w][cur], run);
   __syncthreads();
   for (int dg = threadIdx.x; dg < kDigits; dg += kSortThreads) {
     unsigned tot = 0;
@@ -586,7 +614,7 @@ struct StageMeta {
 constexpr int kRedWarps = 4;  // warps per reduce block
 
 template <typename TW, int G, int VW, int NCB, int U>
-__global__ void __launch_bounds__(kRedWarps * 32) segreduce_adagrad_kernel(
+__global__ void __launch_bounds__(kRedWarps * 32, 8) segreduce_adagrad_kernel(
     TableView t, const unsigned* __restrict__ K, const unsigned* __restrict__ V, const float* __restrict__ scale,
     int mean, const float* __restrict__ grad, unsigned n, unsigned n_bags, unsigned n_chunks,
     float* __restrict__ partA, float* __restrict__ partB, unsigned* __restrict__ arow, float lr, float eps) {
@@ -881,7 +909,7 @@ template <typename TW, int G, int VW, int NCB>
 static cudaError_t launch_reduce(const emb_table* t, const unsigned* K, const unsigned* V, const float* scale,
                                  int mean, const float* grad, unsigned n, unsigned n_bags, const WsLayout& L, char* ws,
                                  float lr, float eps, cudaStream_t st) {
-  constexpr int U = (VW == 8 ? 4 : 8) / NCB;  // 128 bytes of grad_out in flight per lane
+  constexpr int U = NCB >= 4 ? 1 : 4 / NCB;  // grad_out vectors in flight per lane (measured best at 4)
   constexpr int P = 32 / G;
   TableView v = t->view();
   const int threads = kRedWarps * 32;
@@ -905,26 +933,16 @@ static cudaError_t launch_reduce(const emb_table* t, const unsigned* K, const un
   return cudaGetLastError();
 }
 
-// Lanes per row: one vector of VW grad_out floats per lane (32-byte vectors
-// when every dim and the grad_out pointer allow it), up to 32 lanes; wider
-// rows give each lane several column blocks.
+// Lanes per row: one 16-byte vector of grad_out per lane, up to 32 lanes;
+// wider rows give each lane several column blocks.  (32-byte vectors with
+// half the lanes per row measured slower at 100M keys x dim 128: they cost
+// registers, and resident warps matter more here than load width.)
 template <typename TW>
 static cudaError_t dispatch_reduce(const emb_table* t, const unsigned* K, const unsigned* V, const float* scale,
                                    int mean, const float* grad, unsigned n, unsigned n_bags, const WsLayout& L,
                                    char* ws, float lr, float eps, cudaStream_t st) {
-  bool v8 = ((uintptr_t)grad & 31) == 0;
-  for (const SlotInfo& si : t->sinfo_h) v8 = v8 && (si.dim % 8 == 0);
   const int md = t->st.max_dim;
 #define EMB_RED(G, VW, NCB) return launch_reduce<TW, G, VW, NCB>(t, K, V, scale, mean, grad, n, n_bags, L, ws, lr, eps, st)
-  if (v8) {
-    if (md <= 8) EMB_RED(1, 8, 1);
-    if (md <= 16) EMB_RED(2, 8, 1);
-    if (md <= 32) EMB_RED(4, 8, 1);
-    if (md <= 64) EMB_RED(8, 8, 1);
-    if (md <= 128) EMB_RED(16, 8, 1);
-    if (md <= 256) EMB_RED(32, 8, 1);
-    EMB_RED(32, 8, 2);
-  }
   if (md <= 4) EMB_RED(1, 4, 1);
   if (md <= 8) EMB_RED(2, 4, 1);
   if (md <= 16) EMB_RED(4, 4, 1);

@@ -5,10 +5,11 @@
 // merge"), and FP16 rows are read with vector loads.  JD ads article, 4.2.1:
 // per-sample bags pooled by sum or mean.
 //
-// Mapping (one launch for every slot and dim): one warp per bag, grid-stride
-// over bags in CSR order.  The warp resolves up to 32 keys of the bag at once
-// (one key per lane: the probes of 32 keys are in flight together), then its
-// lanes split into P = 32/G groups of G lanes; group p pools keys p, p+P, ...
+// Mapping (one launch for every slot and dim): one team of TEAM lanes (8, 16
+// or 32: a warp holds 32/TEAM teams) per bag, grid-stride over bags in CSR
+// order.  The team resolves up to TEAM keys of the bag at once (one key per
+// lane: their probes are in flight together), then its lanes split into
+// P = TEAM/G groups of G lanes; group p pools keys p, p+P, ...
 // of the chunk, each lane owning 16-byte column vectors of the row.  U keys
 // per group are gathered before any is added, so every lane keeps U x NCB
 // 16-byte loads in flight.  The P partial sums are combined with xor
@@ -70,15 +71,19 @@ struct Record {
   float* scale;
 };
 
-template <typename TW, int NCB, int U, bool kRecord>
+template <typename TW, int TEAM, int NCB, int U, bool kRecord>
 __global__ void __launch_bounds__(256) fwd_pool_kernel(TableView t, const long long* __restrict__ offsets,
                                                        long long n_bags, const long long* __restrict__ keys,
                                                        long long nnz, int mean, float* __restrict__ out, Record rec) {
   constexpr int VEC = VecOf<TW>::kElems;
+  constexpr int BPW = 32 / TEAM;  // bags a warp works on side by side
   const int lane = threadIdx.x & 31;
-  const long long nwarps = ((long long)gridDim.x * blockDim.x) >> 5;
+  const int team = lane / TEAM, tl = lane % TEAM;
+  const unsigned tmask = TEAM == 32 ? 0xffffffffu : (((1u << TEAM) - 1u) << (team * TEAM));
+  const long long nteams = (((long long)gridDim.x * blockDim.x) >> 5) * BPW;
   const TW* W = static_cast<const TW*>(t.W);
-  for (long long bag = (blockIdx.x * (long long)blockDim.x + threadIdx.x) >> 5; bag < n_bags; bag += nwarps) {
+  for (long long bag = ((blockIdx.x * (long long)blockDim.x + threadIdx.x) >> 5) * BPW + team; bag < n_bags;
+       bag += nteams) {
     const int s = (int)((unsigned)bag % (unsigned)t.n_slots);
     const long long b = (unsigned)bag / (unsigned)t.n_slots;
     int D, col;
@@ -94,13 +99,13 @@ __global__ void __launch_bounds__(256) fwd_pool_kernel(TableView t, const long l
       ebase = si.elem_base;
       rbase = si.row_base;
     }
-    const int G = min(32, pow2_at_least(D / VEC));  // lanes per key
-    const int P = 32 / G;                           // keys pooled side by side
-    const int sub = lane / G, li = lane % G;
+    const int G = min(TEAM, pow2_at_least(D / VEC));  // lanes per key
+    const int P = TEAM / G;                           // keys pooled side by side
+    const int sub = tl / G, li = tl % G;
 
     long long start = offsets[bag], end = offsets[bag + 1];
     if (start < 0 || end > nnz || end < start || (bag == 0 && start != 0) || (bag == n_bags - 1 && end != nnz)) {
-      if (lane == 0) atomicOr(t.flags, EMB_FLAG_BAD_OFFSETS);
+      if (tl == 0) atomicOr(t.flags, EMB_FLAG_BAD_OFFSETS);
       start = min(max(start, 0LL), nnz);
       end = min(max(end, start), nnz);
     }
@@ -110,11 +115,11 @@ __global__ void __launch_bounds__(256) fwd_pool_kernel(TableView t, const long l
 #pragma unroll
       for (int j = 0; j < VEC; ++j) acc[c][j] = 0.f;
 
-    for (long long c0 = start; c0 < end; c0 += 32) {
-      const int n = (int)min(32LL, end - c0);
+    for (long long c0 = start; c0 < end; c0 += TEAM) {
+      const int n = (int)min((long long)TEAM, end - c0);
       long long elem = -1;  // first weight element of this lane's key, -1 = miss
-      if (lane < n) {
-        const long long k = keys[c0 + lane];
+      if (tl < n) {
+        const long long k = keys[c0 + tl];
         unsigned row = t.n_rows;
         if (key_slot(k) != s) {
           atomicOr(t.flags, EMB_FLAG_SLOT_MISMATCH);
@@ -127,8 +132,8 @@ __global__ void __launch_bounds__(256) fwd_pool_kernel(TableView t, const long l
           }
         }
         if (kRecord) {
-          rec.K[c0 + lane] = row;
-          rec.V[c0 + lane] = (unsigned)bag;
+          rec.K[c0 + tl] = row;
+          rec.V[c0 + tl] = (unsigned)bag;
         }
       }
       for (int base = 0; base < n; base += P * U) {
@@ -136,7 +141,7 @@ __global__ void __launch_bounds__(256) fwd_pool_kernel(TableView t, const long l
 #pragma unroll
         for (int u = 0; u < U; ++u) {
           const int i = base + u * P + sub;
-          const long long e = __shfl_sync(0xffffffffu, elem, i & 31);
+          const long long e = __shfl_sync(tmask, elem, i & (TEAM - 1), TEAM);
           const bool ok = (i < n) && (e >= 0);
 #pragma unroll
           for (int c = 0; c < NCB; ++c) {
@@ -150,14 +155,14 @@ __global__ void __launch_bounds__(256) fwd_pool_kernel(TableView t, const long l
           for (int c = 0; c < NCB; ++c) VecOf<TW>::add(acc[c], v[u][c]);
       }
     }
-    // combine the P key groups (fixed xor tree: deterministic)
+    // combine the P key groups of the team (fixed xor tree: deterministic)
 #pragma unroll
     for (int c = 0; c < NCB; ++c)
 #pragma unroll
       for (int j = 0; j < VEC; ++j)
-        for (int off = G; off < 32; off <<= 1) acc[c][j] += __shfl_xor_sync(0xffffffffu, acc[c][j], off);
+        for (int off = G; off < TEAM; off <<= 1) acc[c][j] += __shfl_xor_sync(tmask, acc[c][j], off, TEAM);
 
-    if (kRecord && mean && lane == 0) rec.scale[bag] = end > start ? 1.0f / (float)(end - start) : 0.f;
+    if (kRecord && mean && tl == 0) rec.scale[bag] = end > start ? 1.0f / (float)(end - start) : 0.f;
     if (sub == 0) {
       const long long L = end - start;
       const float den = (mean && L > 0) ? (float)L : 1.f;  // mean over L counting misses; L = 0 gives 0
@@ -176,24 +181,37 @@ __global__ void __launch_bounds__(256) fwd_pool_kernel(TableView t, const long l
   }
 }
 
+// Lanes per bag.  Teams of 8 or 16 lanes (several short bags per warp) were
+// measured slower than one bag per warp at 100M keys x dim 128 (the probes of
+// 32 keys in flight per bag matter more than idle lanes on short bags), so
+// every table uses 32; the narrower teams stay available to the launcher.
+static int fwd_team(int /*max_vecs*/) { return 32; }
+
 template <typename TW, bool kRecord>
 static cudaError_t launch_fwd(const emb_table* t, const long long* offsets, long long n_bags, const long long* keys,
                               long long nnz, int mean, float* out, Record rec, cudaStream_t st) {
   constexpr int VEC = VecOf<TW>::kElems;
-  const int max_vecs = t->st.max_dim / VEC;      // 16-byte vectors in the widest row
-  const int ncb = (max_vecs + 31) / 32;          // column blocks per lane at G = 32
+  const int max_vecs = t->st.max_dim / VEC;  // 16-byte vectors in the widest row
+  const int team = fwd_team(max_vecs);
+  const int ncb = (max_vecs + team - 1) / team;  // column blocks per lane
   const int threads = 256;
-  long long blocks = (n_bags * 32 + threads - 1) / threads;
+  long long blocks = (n_bags * team + threads - 1) / threads;
   const long long resident = (long long)sm_count() * (2048 / threads);
   if (blocks > resident) blocks = resident;
   if (blocks < 1) blocks = 1;
   TableView v = t->view();
-  if (ncb <= 1)
-    fwd_pool_kernel<TW, 1, 4, kRecord><<<(int)blocks, threads, 0, st>>>(v, offsets, n_bags, keys, nnz, mean, out, rec);
-  else if (ncb <= 2)
-    fwd_pool_kernel<TW, 2, 2, kRecord><<<(int)blocks, threads, 0, st>>>(v, offsets, n_bags, keys, nnz, mean, out, rec);
-  else
-    fwd_pool_kernel<TW, 4, 1, kRecord><<<(int)blocks, threads, 0, st>>>(v, offsets, n_bags, keys, nnz, mean, out, rec);
+#define EMB_FWD(TM, NC, UU) \
+  fwd_pool_kernel<TW, TM, NC, UU, kRecord><<<(int)blocks, threads, 0, st>>>(v, offsets, n_bags, keys, nnz, mean, out, rec)
+  if (team == 8) {
+    if (ncb <= 1) EMB_FWD(8, 1, 4); else EMB_FWD(8, 2, 2);
+  } else if (team == 16) {
+    if (ncb <= 1) EMB_FWD(16, 1, 4); else EMB_FWD(16, 2, 2);
+  } else {
+    if (ncb <= 1) EMB_FWD(32, 1, 4);
+    else if (ncb <= 2) EMB_FWD(32, 2, 2);
+    else EMB_FWD(32, 4, 1);
+  }
+#undef EMB_FWD
   return cudaGetLastError();
 }
 
