@@ -971,7 +971,6 @@ static emb_status run_bwd(emb_table* table, const int64_t* offsets_d, int64_t n_
                           int64_t nnz, emb_pool pool, const float* grad_out_d, float lr, float eps, char* ws,
                           const WsLayout& L, cudaStream_t st, bool recorded = false) {
   const unsigned n = (unsigned)nnz;
-  const unsigned miss = (unsigned)table->st.n_keys;
   // grad_out rows are addressed as 32-bit float4 indices
   if ((unsigned long long)(n_bags / table->st.n_slots) * (unsigned long long)table->st.sum_dims >= (1ULL << 34))
     return fail(EMB_ERR_UNSUPPORTED, "grad_out larger than 2^34 elements");
