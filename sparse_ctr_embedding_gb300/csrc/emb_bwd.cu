@@ -275,7 +275,7 @@ __device__ __forceinline__ unsigned block_excl_scan(unsigned v, unsigned* sm) {
   return sm[w] + x - v;
 }
 
-__global__ void __launch_bounds__(kSortThreads) radix_scatter_kernel(
+__global__ void __launch_bounds__(kSortThreads, 3) radix_scatter_kernel(
     const unsigned* __restrict__ kin, const unsigned* __restrict__ vin, unsigned* __restrict__ kout,
     unsigned* __restrict__ vout, unsigned n, int shift, const unsigned* __restrict__ counts, unsigned n_tiles) {
   extern __shared__ unsigned smem[];
