@@ -35,6 +35,7 @@
 #include <algorithm>
 #include <cstdio>
 #include <mutex>
+#include <type_traits>
 
 #include "emb_internal.cuh"
 
@@ -72,7 +73,7 @@ struct WsHeader {
 static size_t align_up(size_t x) { return (x + 255) & ~(size_t)255; }
 
 struct WsLayout {
-  size_t hdr, kA, kB, vA, vB, scale, counts, partials, partA, partB, arow, uniq, total;
+  size_t hdr, kA, kB, vA, vB, scale, counts, partials, partA, partB, arow, zero, uniq, total;
   unsigned n_tiles_sort, n_chunks, n_scan_partials;
   int max_dim;
 };
@@ -103,6 +104,7 @@ static WsLayout ws_layout(const emb_table* t, long long n_bags, long long nnz) {
   L.partA = take((size_t)L.n_chunks * L.max_dim * 4);
   L.partB = take((size_t)L.n_chunks * L.max_dim * 4);
   L.arow = take((size_t)L.n_chunks * 4);
+  L.zero = take((size_t)L.max_dim * 4);  // a zero grad_out row for positions that add nothing
   L.uniq = L.kA;  // emb_bwd_unique_keys reuses the buffer that is not holding the sorted keys
   L.total = o;
   return L;
@@ -616,8 +618,9 @@ constexpr int kRedWarps = 4;  // warps per reduce block
 template <typename TW, int G, int VW, int NCB, int U>
 __global__ void __launch_bounds__(kRedWarps * 32, 8) segreduce_adagrad_kernel(
     TableView t, const unsigned* __restrict__ K, const unsigned* __restrict__ V, const float* __restrict__ scale,
-    int mean, const float* __restrict__ grad, unsigned n, unsigned n_bags, unsigned n_chunks,
-    float* __restrict__ partA, float* __restrict__ partB, unsigned* __restrict__ arow, float lr, float eps) {
+    int mean, const float* __restrict__ grad, const float* __restrict__ zrow, unsigned n, unsigned n_bags,
+    unsigned n_chunks, float* __restrict__ partA, float* __restrict__ partB, unsigned* __restrict__ arow, float lr,
+    float eps) {
   constexpr int P = 32 / G;
   constexpr int CW = G * VW * NCB;      // columns a group covers
   constexpr int kStage = U + 1;
@@ -726,31 +729,31 @@ __global__ void __launch_bounds__(kRedWarps * 32, 8) segreduce_adagrad_kernel(
         const RowGeo g = geo_from_slot(t, kk, sj);
         if (g.ok) prefetch_row<TW>(t, g);
       }
-      // ---- in-order walk, U positions in flight per lane
-      for (int j0 = 0; j0 < m; j0 += U) {
+      // ---- in-order walk, U positions in flight per lane.  Full windows (all
+      // but a sub-chunk's last) take a path without per-position bound tests.  Positions that contribute nothing (merged duplicates,
+      // misses, lanes past a ragged row's dim) read the zero row instead of
+      // predicating the load.
+      auto step = [&](const int j0, auto full_c) {
+        constexpr bool kFull = decltype(full_c)::value;
         GradVec<VW> gv[U][NCB];
 #pragma unroll
         for (int u = 0; u < U; ++u) {
-          const int src = (j0 + u) & (G - 1);
+          const int j = j0 + u;
+          const int src = j & (G - 1);
           const unsigned gj = __shfl_sync(gmask, go, src, G);
           const int dj = udim ? udim : __shfl_sync(gmask, Dj, src, G);
-          const bool live = j0 + u < m && gj != kSkip;
+          const bool live = (kFull || j < m) && gj != kSkip;
 #pragma unroll
           for (int cc = 0; cc < NCB; ++cc) {
             const int q = cc * G + li;
-            if (live && q * VW < dj) {
-              gv[u][cc].load(grad + ((size_t)gj + q) * VW);
-            } else {
-#pragma unroll
-              for (int j = 0; j < VW; ++j) gv[u][cc].v[j] = 0.f;
-            }
+            gv[u][cc].load((live && q * VW < dj) ? grad + ((size_t)gj + q) * VW : zrow);
           }
         }
         int ns = 0;
 #pragma unroll
         for (int u = 0; u < U; ++u) {
           const int j = j0 + u;
-          if (j >= m) break;
+          if (!kFull && j >= m) break;
           if ((smask >> j) & 1u) {
             if (cur != kNoRow) stage_cur(ns++, true);
             cur = __shfl_sync(gmask, kk, j, G);
@@ -767,6 +770,12 @@ __global__ void __launch_bounds__(kRedWarps * 32, 8) segreduce_adagrad_kernel(
           for (int cc = 0; cc < NCB; ++cc) fma_x2<VW>(acc[cc], wj, gv[u][cc].v);
         }
         if (ns) drain(ns);
+      };
+      if (m == G) {
+#pragma unroll 1  // unrolling the window overflows the instruction cache (measured 2.4x slower)
+        for (int j0 = 0; j0 < G; j0 += U) step(j0, std::true_type{});
+      } else {
+        for (int j0 = 0; j0 < m; j0 += U) step(j0, std::false_type{});
       }
     }
     if (cur != kNoRow) {
@@ -920,8 +929,11 @@ static cudaError_t launch_reduce(const emb_table* t, const unsigned* K, const un
   float* pa = (float*)(ws + L.partA);
   float* pb = (float*)(ws + L.partB);
   unsigned* ar = (unsigned*)(ws + L.arow);
+  float* zrow = (float*)(ws + L.zero);
+  cudaError_t e = cudaMemsetAsync(zrow, 0, (size_t)L.max_dim * 4, st);
+  if (e != cudaSuccess) return e;
   segreduce_adagrad_kernel<TW, G, VW, NCB, U><<<(int)std::max(1LL, blocks), threads, 0, st>>>(
-      v, K, V, scale, mean, grad, n, n_bags, L.n_chunks, pa, pb, ar, lr, eps);
+      v, K, V, scale, mean, grad, zrow, n, n_bags, L.n_chunks, pa, pb, ar, lr, eps);
   mark_phase(t, 2, st);
   // the fixup reads partial rows four columns per lane
   constexpr int G4 = G * VW / 4 > 32 ? 32 : G * VW / 4;
