@@ -45,7 +45,7 @@ emb_status check_batch(const emb_table* t, const int64_t* offsets_d, int64_t n_b
                        int64_t nnz, int pool);
 cudaError_t launch_forward(const emb_table* t, const long long* offsets, long long n_bags, const long long* keys,
                            long long nnz, int mean, float* out, unsigned* K, unsigned* V, float* scale,
-                           cudaStream_t st);
+                           unsigned long long* work, cudaStream_t st);
 
 constexpr int kChunk = 512;                      // sorted positions per reduce sub-chunk
 constexpr int kSortWarps = 8;
@@ -73,7 +73,7 @@ struct WsHeader {
 static size_t align_up(size_t x) { return (x + 255) & ~(size_t)255; }
 
 struct WsLayout {
-  size_t hdr, kA, kB, vA, vB, scale, counts, partials, partA, partB, arow, zero, uniq, total;
+  size_t hdr, kA, kB, vA, vB, scale, counts, partials, partA, partB, arow, zero, work, fwork, uniq, total;
   unsigned n_tiles_sort, n_chunks, n_scan_partials;
   int max_dim;
 };
@@ -105,6 +105,8 @@ static WsLayout ws_layout(const emb_table* t, long long n_bags, long long nnz) {
   L.partB = take((size_t)L.n_chunks * L.max_dim * 4);
   L.arow = take((size_t)L.n_chunks * 4);
   L.zero = take((size_t)L.max_dim * 4);  // a zero grad_out row for positions that add nothing
+  L.work = take(sizeof(unsigned));        // sub-chunk counter of the reduce
+  L.fwork = take(sizeof(unsigned long long));  // bag counter of the recording forward
   L.uniq = L.kA;  // emb_bwd_unique_keys reuses the buffer that is not holding the sorted keys
   L.total = o;
   return L;
@@ -455,6 +457,59 @@ __device__ __forceinline__ void stw4(__half* p, const float (&v)[4]) {
   *reinterpret_cast<uint2*>(p) = x;
 }
 
+// L2 eviction-priority policies (createpolicy) for loads and stores that
+// carry a cache hint.
+__device__ __forceinline__ unsigned long long l2_evict_last() {
+  unsigned long long p;
+  asm("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(p));
+  return p;
+}
+__device__ __forceinline__ unsigned long long l2_evict_first() {
+  unsigned long long p;
+  asm("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));
+  return p;
+}
+__device__ __forceinline__ float4 ldg_hint(const float* p, unsigned long long pol) {
+  float4 v;
+  asm("ld.global.nc.L2::cache_hint.v4.f32 {%0,%1,%2,%3}, [%4], %5;"
+      : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
+      : "l"(p), "l"(pol));
+  return v;
+}
+__device__ __forceinline__ float4 ld_hint(const float* p, unsigned long long pol) {
+  float4 v;
+  asm volatile("ld.global.L2::cache_hint.v4.f32 {%0,%1,%2,%3}, [%4], %5;"
+               : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
+               : "l"(p), "l"(pol));
+  return v;
+}
+__device__ __forceinline__ void st_hint(float* p, float4 v, unsigned long long pol) {
+  asm volatile("st.global.L2::cache_hint.v4.f32 [%0], {%1,%2,%3,%4}, %5;" ::"l"(p), "f"(v.x), "f"(v.y), "f"(v.z),
+               "f"(v.w), "l"(pol)
+               : "memory");
+}
+__device__ __forceinline__ void ldw4_hint(const float* p, float (&v)[4], unsigned long long pol) {
+  const float4 x = ld_hint(p, pol);
+  v[0] = x.x; v[1] = x.y; v[2] = x.z; v[3] = x.w;
+}
+__device__ __forceinline__ void ldw4_hint(const __half* p, float (&v)[4], unsigned long long pol) {
+  unsigned a, b;
+  asm volatile("ld.global.L2::cache_hint.v2.u32 {%0,%1}, [%2], %3;" : "=r"(a), "=r"(b) : "l"(p), "l"(pol));
+  const float2 x = __half22float2(*reinterpret_cast<const __half2*>(&a));
+  const float2 y = __half22float2(*reinterpret_cast<const __half2*>(&b));
+  v[0] = x.x; v[1] = x.y; v[2] = y.x; v[3] = y.y;
+}
+__device__ __forceinline__ void stw4_hint(float* p, const float (&v)[4], unsigned long long pol) {
+  st_hint(p, make_float4(v[0], v[1], v[2], v[3]), pol);
+}
+__device__ __forceinline__ void stw4_hint(__half* p, const float (&v)[4], unsigned long long pol) {
+  const __half2 a = __floats2half2_rn(v[0], v[1]);
+  const __half2 b = __floats2half2_rn(v[2], v[3]);
+  asm volatile("st.global.L2::cache_hint.v2.u32 [%0], {%1,%2}, %3;" ::"l"(p), "r"(*reinterpret_cast<const unsigned*>(&a)),
+               "r"(*reinterpret_cast<const unsigned*>(&b)), "l"(pol)
+               : "memory");
+}
+
 // One element of the Adagrad update:  acc += g*g;  w -= lr*g / (sqrt(acc) + eps).
 // sqrt(acc) is acc * rsqrt(acc) and the quotient a fast divide (hardware
 // reciprocal square root and reciprocal, each within a few ulp), which keeps
@@ -620,7 +675,7 @@ __global__ void __launch_bounds__(kRedWarps * 32, 8) segreduce_adagrad_kernel(
     TableView t, const unsigned* __restrict__ K, const unsigned* __restrict__ V, const float* __restrict__ scale,
     int mean, const float* __restrict__ grad, const float* __restrict__ zrow, unsigned n, unsigned n_bags,
     unsigned n_chunks, float* __restrict__ partA, float* __restrict__ partB, unsigned* __restrict__ arow, float lr,
-    float eps) {
+    float eps, unsigned* __restrict__ work) {
   constexpr int P = 32 / G;
   constexpr int CW = G * VW * NCB;      // columns a group covers
   constexpr int kStage = U + 1;
@@ -638,7 +693,15 @@ __global__ void __launch_bounds__(kRedWarps * 32, 8) segreduce_adagrad_kernel(
   float(*st)[CW] = stage[wid][sub];
   StageMeta* mt = meta[wid][sub];
   const unsigned n_groups = ((gridDim.x * blockDim.x) >> 5) * P;
-  for (unsigned c = ((blockIdx.x * blockDim.x + threadIdx.x) >> 5) * P + sub; c < n_chunks; c += n_groups) {
+  // sub-chunks: a static grid-stride order, or (work != NULL) taken in order from a counter
+  auto next_chunk = [&](unsigned c) -> unsigned {
+    if (!work) return c + n_groups;
+    unsigned v = 0;
+    if (li == 0) v = atomicAdd(work, 1u);
+    return __shfl_sync(gmask, v, 0, G);
+  };
+  const unsigned c_first = work ? next_chunk(0) : ((blockIdx.x * blockDim.x + threadIdx.x) >> 5) * P + sub;
+  for (unsigned c = c_first; c < n_chunks; c = next_chunk(c)) {
     const unsigned cs = c * kChunk;
     const unsigned ce = min(cs + kChunk, n);
     const unsigned before = cs > 0 ? K[cs - 1] : kNoRow;
@@ -932,8 +995,15 @@ static cudaError_t launch_reduce(const emb_table* t, const unsigned* K, const un
   float* zrow = (float*)(ws + L.zero);
   cudaError_t e = cudaMemsetAsync(zrow, 0, (size_t)L.max_dim * 4, st);
   if (e != cudaSuccess) return e;
+  // sub-chunks are handed out in order from a counter: all resident groups
+  // then work inside a narrow window of one feature slot, whose grad_out
+  // columns stay in L2 (measured 23.3 -> 17.2 ms against a static grid-stride
+  // order at 100M keys x dim 128)
+  unsigned* work = (unsigned*)(ws + L.work);
+  e = cudaMemsetAsync(work, 0, sizeof(unsigned), st);
+  if (e != cudaSuccess) return e;
   segreduce_adagrad_kernel<TW, G, VW, NCB, U><<<(int)std::max(1LL, blocks), threads, 0, st>>>(
-      v, K, V, scale, mean, grad, zrow, n, n_bags, L.n_chunks, pa, pb, ar, lr, eps);
+      v, K, V, scale, mean, grad, zrow, n, n_bags, L.n_chunks, pa, pb, ar, lr, eps, work);
   mark_phase(t, 2, st);
   // the fixup reads partial rows four columns per lane
   constexpr int G4 = G * VW / 4 > 32 ? 32 : G * VW / 4;
@@ -1102,9 +1172,13 @@ emb_status emb_lookup_fwd_record(emb_table* table, const int64_t* offsets_d, int
   ws_header_kernel<<<1, 1, 0, st>>>((WsHeader*)(ws + L.hdr), (unsigned)nnz, (unsigned)n_bags,
                                     (unsigned)(sort_passes(table) & 1), (unsigned)table->st.n_keys);
   if (n_bags > 0) {
+    // bags are handed out in order from a counter (measured 17.7 -> 15.1 ms at
+    // 100M keys x dim 128 against a static order; Zipf bag lengths unbalance it)
+    unsigned long long* fwork = (unsigned long long*)(ws + L.fwork);
+    EMB_CUDA(cudaMemsetAsync(fwork, 0, sizeof(unsigned long long), st));
     cudaError_t e = launch_forward(table, (const long long*)offsets_d, n_bags, (const long long*)keys_d, nnz,
                                    pool == EMB_POOL_MEAN, out_d, (unsigned*)(ws + L.kA), (unsigned*)(ws + L.vA),
-                                   (float*)(ws + L.scale), st);
+                                   (float*)(ws + L.scale), fwork, st);
     if (e != cudaSuccess) return cuda_fail(e, "fwd_pool_kernel launch");
   }
   EMB_CUDA(cudaGetLastError());

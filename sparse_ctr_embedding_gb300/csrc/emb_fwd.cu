@@ -71,7 +71,10 @@ struct Record {
   unsigned* K;
   unsigned* V;
   float* scale;
+  unsigned long long* work;  // optional bag counter: bags taken in batches, in order
 };
+
+constexpr int kBagBatch = 32;  // bags per counter increment
 
 // Bounded to 8 resident blocks (full occupancy): the gathers are latency
 // bound, and resident warps beat registers (measured at 100M keys x dim 128).
@@ -86,8 +89,24 @@ __global__ void __launch_bounds__(256, 8) fwd_pool_kernel(TableView t, const lon
   const unsigned tmask = TEAM == 32 ? 0xffffffffu : (((1u << TEAM) - 1u) << (team * TEAM));
   const long long nteams = (((long long)gridDim.x * blockDim.x) >> 5) * BPW;
   const TW* W = static_cast<const TW*>(t.W);
-  for (long long bag = ((blockIdx.x * (long long)blockDim.x + threadIdx.x) >> 5) * BPW + team; bag < n_bags;
-       bag += nteams) {
+  // bags: a static grid-stride order, or batches of kBagBatch consecutive bags
+  // taken in order from a counter (balances warps over bags of very
+  // different lengths)
+  long long stat = ((blockIdx.x * (long long)blockDim.x + threadIdx.x) >> 5) * BPW + team;
+  for (;;) {
+    long long b_lo, b_hi;
+    if (rec.work) {
+      unsigned long long v = 0;
+      if (tl == 0) v = atomicAdd(rec.work, (unsigned long long)kBagBatch);
+      b_lo = (long long)__shfl_sync(tmask, v, 0, TEAM);
+      b_hi = min(b_lo + kBagBatch, n_bags);
+    } else {
+      b_lo = stat;
+      b_hi = stat + 1;
+      stat += nteams;
+    }
+    if (b_lo >= n_bags) break;
+  for (long long bag = b_lo; bag < b_hi; ++bag) {
     const int s = (int)((unsigned)bag % (unsigned)t.n_slots);
     const long long b = (unsigned)bag / (unsigned)t.n_slots;
     int D, col;
@@ -183,6 +202,7 @@ __global__ void __launch_bounds__(256, 8) fwd_pool_kernel(TableView t, const lon
       }
     }
   }
+  }
 }
 
 // Lanes per bag.  Teams of 8 or 16 lanes (several short bags per warp) were
@@ -226,8 +246,8 @@ static cudaError_t launch_fwd(const emb_table* t, const long long* offsets, long
 // Forward launch, optionally recording (row, bag) pairs for the backward.
 cudaError_t launch_forward(const emb_table* t, const long long* offsets, long long n_bags, const long long* keys,
                            long long nnz, int mean, float* out, unsigned* K, unsigned* V, float* scale,
-                           cudaStream_t st) {
-  const Record rec{K, V, scale};
+                           unsigned long long* work, cudaStream_t st) {
+  const Record rec{K, V, scale, work};
   const bool record = K != nullptr;
   if (t->st.wdtype == EMB_F16)
     return record ? launch_fwd<__half, true>(t, offsets, n_bags, keys, nnz, mean, out, rec, st)
@@ -260,7 +280,7 @@ extern "C" emb_status emb_lookup_fwd(emb_table* table, const int64_t* offsets_d,
   if (!out_d) return fail(EMB_ERR_INVALID_ARG, "out is NULL");
   cudaStream_t st = (cudaStream_t)stream;
   cudaError_t e = launch_forward(table, (const long long*)offsets_d, n_bags, (const long long*)keys_d, nnz,
-                                 pool == EMB_POOL_MEAN, out_d, nullptr, nullptr, nullptr, st);
+                                 pool == EMB_POOL_MEAN, out_d, nullptr, nullptr, nullptr, nullptr, st);
   if (e != cudaSuccess) return cuda_fail(e, "fwd_pool_kernel launch");
   return EMB_OK;
 }
