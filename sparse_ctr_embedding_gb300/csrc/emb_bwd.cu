@@ -457,59 +457,6 @@ __device__ __forceinline__ void stw4(__half* p, const float (&v)[4]) {
   *reinterpret_cast<uint2*>(p) = x;
 }
 
-// L2 eviction-priority policies (createpolicy) for loads and stores that
-// carry a cache hint.
-__device__ __forceinline__ unsigned long long l2_evict_last() {
-  unsigned long long p;
-  asm("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(p));
-  return p;
-}
-__device__ __forceinline__ unsigned long long l2_evict_first() {
-  unsigned long long p;
-  asm("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));
-  return p;
-}
-__device__ __forceinline__ float4 ldg_hint(const float* p, unsigned long long pol) {
-  float4 v;
-  asm("ld.global.nc.L2::cache_hint.v4.f32 {%0,%1,%2,%3}, [%4], %5;"
-      : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
-      : "l"(p), "l"(pol));
-  return v;
-}
-__device__ __forceinline__ float4 ld_hint(const float* p, unsigned long long pol) {
-  float4 v;
-  asm volatile("ld.global.L2::cache_hint.v4.f32 {%0,%1,%2,%3}, [%4], %5;"
-               : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
-               : "l"(p), "l"(pol));
-  return v;
-}
-__device__ __forceinline__ void st_hint(float* p, float4 v, unsigned long long pol) {
-  asm volatile("st.global.L2::cache_hint.v4.f32 [%0], {%1,%2,%3,%4}, %5;" ::"l"(p), "f"(v.x), "f"(v.y), "f"(v.z),
-               "f"(v.w), "l"(pol)
-               : "memory");
-}
-__device__ __forceinline__ void ldw4_hint(const float* p, float (&v)[4], unsigned long long pol) {
-  const float4 x = ld_hint(p, pol);
-  v[0] = x.x; v[1] = x.y; v[2] = x.z; v[3] = x.w;
-}
-__device__ __forceinline__ void ldw4_hint(const __half* p, float (&v)[4], unsigned long long pol) {
-  unsigned a, b;
-  asm volatile("ld.global.L2::cache_hint.v2.u32 {%0,%1}, [%2], %3;" : "=r"(a), "=r"(b) : "l"(p), "l"(pol));
-  const float2 x = __half22float2(*reinterpret_cast<const __half2*>(&a));
-  const float2 y = __half22float2(*reinterpret_cast<const __half2*>(&b));
-  v[0] = x.x; v[1] = x.y; v[2] = y.x; v[3] = y.y;
-}
-__device__ __forceinline__ void stw4_hint(float* p, const float (&v)[4], unsigned long long pol) {
-  st_hint(p, make_float4(v[0], v[1], v[2], v[3]), pol);
-}
-__device__ __forceinline__ void stw4_hint(__half* p, const float (&v)[4], unsigned long long pol) {
-  const __half2 a = __floats2half2_rn(v[0], v[1]);
-  const __half2 b = __floats2half2_rn(v[2], v[3]);
-  asm volatile("st.global.L2::cache_hint.v2.u32 [%0], {%1,%2}, %3;" ::"l"(p), "r"(*reinterpret_cast<const unsigned*>(&a)),
-               "r"(*reinterpret_cast<const unsigned*>(&b)), "l"(pol)
-               : "memory");
-}
-
 // One element of the Adagrad update:  acc += g*g;  w -= lr*g / (sqrt(acc) + eps).
 // sqrt(acc) is acc * rsqrt(acc) and the quotient a fast divide (hardware
 // reciprocal square root and reciprocal, each within a few ulp), which keeps
