@@ -158,8 +158,10 @@ EMB_API emb_status emb_table_plan(const emb_table_desc* desc, const int64_t* key
  * bag length L counting misses (L = 0 gives zeros).
  *   offsets_d  int64[n_bags+1] CSR offsets; n_bags must be a multiple of n_slots.
  *   keys_d     int64[nnz].
- *   out_d      float32[n_bags/n_slots, sum_dims], fully overwritten.
- * Errors (host, before any work): INVALID_ARG, UNSUPPORTED.  Offsets outside
+ *   out_d      float32[n_bags/n_slots, sum_dims], fully overwritten; 16-byte
+ *              aligned (rows are written with 16-byte stores).
+ * Errors (host, before any work): INVALID_ARG (also for a misaligned out_d),
+ * UNSUPPORTED.  Offsets outside
  * [0, nnz] are clamped and raise EMB_FLAG_BAD_OFFSETS; a key of another slot
  * is skipped and raises EMB_FLAG_SLOT_MISMATCH.
  */
@@ -177,7 +179,8 @@ EMB_API emb_status emb_bwd_workspace_size(const emb_table* table, int64_t n_bags
  * (stable sort by row, fixed-order segmented sums); then for each hit key and
  * each element:  acc += g*g;  w -= lr*g / (sqrt(acc) + eps)  in float32
  * (half weights rounded to nearest-even).  Rows not hit are not touched.
- *   grad_out_d   float32[n_bags/n_slots, sum_dims].
+ *   grad_out_d   float32[n_bags/n_slots, sum_dims], 16-byte aligned (read with
+ *                16-byte vector loads; INVALID_ARG otherwise).
  *   workspace_d  device scratch of at least emb_bwd_workspace_size() bytes,
  *                256-byte aligned; after the call it holds the unique rows of
  *                this step (read them with emb_bwd_unique_keys).

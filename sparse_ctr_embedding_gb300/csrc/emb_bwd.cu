@@ -104,7 +104,7 @@ static WsLayout ws_layout(const emb_table* t, long long n_bags, long long nnz) {
   L.partA = take((size_t)L.n_chunks * L.max_dim * 4);
   L.partB = take((size_t)L.n_chunks * L.max_dim * 4);
   L.arow = take((size_t)L.n_chunks * 4);
-  L.zero = take((size_t)L.max_dim * 4);  // a zero grad_out row for positions that add nothing
+  L.zero = take((size_t)EMB_MAX_DIM * 4);  // a zero grad_out row (the widest lane group) for positions that add nothing
   L.work = take(sizeof(unsigned));        // sub-chunk counter of the reduce
   L.fwork = take(sizeof(unsigned long long));  // bag counter of the recording forward
   L.uniq = L.kA;  // emb_bwd_unique_keys reuses the buffer that is not holding the sorted keys
@@ -607,17 +607,32 @@ struct StageMeta {
 // each lane owns VW-float column vectors (NCB of them) of the row.  Per
 // window of G positions the lanes first work in parallel, one position each:
 // row, bag, merged run of equal (row, bag) neighbours, its weight (1/L times
-// the run length), the index of its grad_out row, and whether a new row
-// starts there; lanes that start a row prefetch its weights and
-// accumulators into L2.  The group then walks the window in order, U
-// positions at a time: one shuffle and one vector load per position and
-// lane, packed multiply-adds, and at a row start the finished row is staged
-// in shared memory.  Staged rows are then applied (Adagrad on a whole
-// segment) or parked (partial of a segment cut by a sub-chunk edge) by one
-// copy of that code, outside the unrolled walk.
+// the run length), the address of its grad_out columns, and whether a new
+// row starts there; each lane leaves that as a 16-byte record in shared
+// memory, and lanes that start a row prefetch its weights and accumulators
+// into L2.  The group then walks the window in order, U positions at a time:
+// per position one broadcast read of the record and one vector load per
+// column block, then multiply-adds; a group of U positions with no row start
+// in it adds without any per-position test.  At a row start the finished row
+// is staged in shared memory.  Staged rows are then applied (Adagrad on a
+// whole segment) or parked (partial of a segment cut by a sub-chunk edge) by
+// one copy of that code, outside the unrolled walk.
 constexpr int kRedWarps = 4;  // warps per reduce block
 
-template <typename TW, int G, int VW, int NCB, int U>
+struct alignas(16) PosRec {
+  const float* p;  // the position's grad_out columns, or the zero row for a position that adds nothing
+  float w;         // its weight: (1/L or 1) x the run of equal (row, bag) positions it stands for, or 0
+  int D;           // dim of its slot (columns at or past it read the zero row)
+};
+
+// acc[i] += w * g[i] for VW columns.
+template <int VW>
+__device__ __forceinline__ void fma_vw(float* acc, float w, const float* g) {
+  fma_x2<VW>(acc, w, g);
+}
+
+// kAllCols: every lane column is inside every row (one dim, equal to G x VW x NCB).
+template <typename TW, int G, int VW, int NCB, int U, bool kAllCols>
 __global__ void __launch_bounds__(kRedWarps * 32, 8) segreduce_adagrad_kernel(
     TableView t, const unsigned* __restrict__ K, const unsigned* __restrict__ V, const float* __restrict__ scale,
     int mean, const float* __restrict__ grad, const float* __restrict__ zrow, unsigned n, unsigned n_bags,
@@ -625,10 +640,11 @@ __global__ void __launch_bounds__(kRedWarps * 32, 8) segreduce_adagrad_kernel(
     float eps, unsigned* __restrict__ work) {
   constexpr int P = 32 / G;
   constexpr int CW = G * VW * NCB;      // columns a group covers
-  constexpr int kStage = U + 1;
-  constexpr unsigned kSkip = 0xFFFFFFFFu;
+  constexpr int UW = U < G ? U : G;     // positions per walk step (a window holds G)
+  constexpr int kStage = UW + 1;
   __shared__ __align__(16) float stage[kRedWarps][P][kStage][CW];
   __shared__ StageMeta meta[kRedWarps][P][kStage];
+  __shared__ PosRec recs[kRedWarps][P][G];
   const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
   const int sub = lane / G, li = lane % G;
   const unsigned gmask = G == 32 ? 0xffffffffu : (((1u << G) - 1u) << (sub * G));
@@ -639,6 +655,7 @@ __global__ void __launch_bounds__(kRedWarps * 32, 8) segreduce_adagrad_kernel(
   const int udim = t.uniform_dim;
   float(*st)[CW] = stage[wid][sub];
   StageMeta* mt = meta[wid][sub];
+  PosRec* rc = recs[wid][sub];
   const unsigned n_groups = ((gridDim.x * blockDim.x) >> 5) * P;
   // sub-chunks: a static grid-stride order, or (work != NULL) taken in order from a counter
   auto next_chunk = [&](unsigned c) -> unsigned {
@@ -722,71 +739,74 @@ __global__ void __launch_bounds__(kRedWarps * 32, 8) segreduce_adagrad_kernel(
       const bool use = valid && !dup && kk < miss && vv < n_bags;
       const bool start = valid && (kk != kp || (i0 == cs && li == 0));
       const unsigned smask = (__ballot_sync(gmask, start) >> (sub * G)) & gbits;
-      int sj = 0, Dj = udim;
-      unsigned go = kSkip;  // index, in VW-float vectors, of this position's grad_out columns
-      if (use) {
-        if (udim) {
-          go = vv * (unsigned)(udim / VW);   // (b*S + s) * D = b * sum_dims + s * D
-        } else {
-          sj = (int)(vv % S);
-          const SlotInfo si = t.sinfo[sj];
-          Dj = si.dim;
-          go = (unsigned)(((unsigned long long)(vv / S) * (unsigned)t.sum_dims + (unsigned)si.col) / VW);
+      int sj = 0;
+      {
+        PosRec r{zrow, 0.f, CW};
+        if (use) {
+          if (udim) {
+            r.p = grad + (size_t)vv * (unsigned)udim;   // (b*S + s) * D = b * sum_dims + s * D
+            r.D = udim;
+          } else {
+            sj = (int)(vv % S);
+            const SlotInfo si = t.sinfo[sj];
+            r.p = grad + (size_t)(vv / S) * (unsigned)t.sum_dims + (unsigned)si.col;
+            r.D = si.dim;
+          }
+          r.w = (mean ? scale[vv] : 1.f) * (float)(nxt - li);
         }
+        rc[li] = r;
       }
-      const float w = use ? (mean ? scale[vv] : 1.f) * (float)(nxt - li) : 0.f;
       if (use && start) {
         const RowGeo g = geo_from_slot(t, kk, sj);
         if (g.ok) prefetch_row<TW>(t, g);
       }
-      // ---- in-order walk, U positions in flight per lane.  Full windows (all
-      // but a sub-chunk's last) take a path without per-position bound tests.  Positions that contribute nothing (merged duplicates,
-      // misses, lanes past a ragged row's dim) read the zero row instead of
-      // predicating the load.
-      auto step = [&](const int j0, auto full_c) {
-        constexpr bool kFull = decltype(full_c)::value;
-        GradVec<VW> gv[U][NCB];
+      __syncwarp(gmask);
+      // ---- in-order walk, U positions in flight per lane.  Positions past
+      // the window's end hold dead records (zero row, weight 0), so every
+      // window walks all G positions without bound tests.
+#pragma unroll 1  // unrolling the window overflows the instruction cache (measured 2.4x slower)
+      for (int j0 = 0; j0 < G; j0 += UW) {
+        GradVec<VW> gv[UW][NCB];
+        float wv[UW];
 #pragma unroll
-        for (int u = 0; u < U; ++u) {
-          const int j = j0 + u;
-          const int src = j & (G - 1);
-          const unsigned gj = __shfl_sync(gmask, go, src, G);
-          const int dj = udim ? udim : __shfl_sync(gmask, Dj, src, G);
-          const bool live = (kFull || j < m) && gj != kSkip;
+        for (int u = 0; u < UW; ++u) {
+          const PosRec r = rc[j0 + u];
+          wv[u] = r.w;
 #pragma unroll
           for (int cc = 0; cc < NCB; ++cc) {
-            const int q = cc * G + li;
-            gv[u][cc].load((live && q * VW < dj) ? grad + ((size_t)gj + q) * VW : zrow);
+            const int q = (cc * G + li) * VW;
+            gv[u][cc].load((kAllCols || q < r.D) ? r.p + q : zrow + q);
           }
         }
-        int ns = 0;
+        const unsigned grp = (smask >> j0) & ((1u << UW) - 1u);
+        if (grp == 0) {
 #pragma unroll
-        for (int u = 0; u < U; ++u) {
-          const int j = j0 + u;
-          if (!kFull && j >= m) break;
-          if ((smask >> j) & 1u) {
-            if (cur != kNoRow) stage_cur(ns++, true);
-            cur = __shfl_sync(gmask, kk, j, G);
-            const unsigned bag = __shfl_sync(gmask, vv, j, G);
-            cur_starts = (i0 + j > cs) || first_starts;
-            cg = (cur < miss && bag < n_bags) ? geo_from_slot(t, cur, (int)(bag % S)) : RowGeo{0, 0, 0, false};
+          for (int u = 0; u < UW; ++u)
 #pragma unroll
-            for (int cc = 0; cc < NCB; ++cc)
+            for (int cc = 0; cc < NCB; ++cc) fma_vw<VW>(acc[cc], wv[u], gv[u][cc].v);
+        } else {
+          int ns = 0;
 #pragma unroll
-              for (int q = 0; q < VW; ++q) acc[cc][q] = 0.f;
+          for (int u = 0; u < UW; ++u) {
+            const int j = j0 + u;
+            if ((grp >> u) & 1u) {
+              if (cur != kNoRow) stage_cur(ns++, true);
+              cur = __shfl_sync(gmask, kk, j, G);
+              const unsigned bag = __shfl_sync(gmask, vv, j, G);
+              cur_starts = (i0 + j > cs) || first_starts;
+              cg = (cur < miss && bag < n_bags) ? geo_from_slot(t, cur, (int)(bag % S)) : RowGeo{0, 0, 0, false};
+#pragma unroll
+              for (int cc = 0; cc < NCB; ++cc)
+#pragma unroll
+                for (int q = 0; q < VW; ++q) acc[cc][q] = 0.f;
+            }
+#pragma unroll
+            for (int cc = 0; cc < NCB; ++cc) fma_vw<VW>(acc[cc], wv[u], gv[u][cc].v);
           }
-          const float wj = __shfl_sync(gmask, w, j, G);
-#pragma unroll
-          for (int cc = 0; cc < NCB; ++cc) fma_x2<VW>(acc[cc], wj, gv[u][cc].v);
+          if (ns) drain(ns);
         }
-        if (ns) drain(ns);
-      };
-      if (m == G) {
-#pragma unroll 1  // unrolling the window overflows the instruction cache (measured 2.4x slower)
-        for (int j0 = 0; j0 < G; j0 += U) step(j0, std::true_type{});
-      } else {
-        for (int j0 = 0; j0 < m; j0 += U) step(j0, std::false_type{});
       }
+      __syncwarp(gmask);  // the next window rewrites the records
     }
     if (cur != kNoRow) {
       stage_cur(0, last_ends);
@@ -933,14 +953,17 @@ static cudaError_t launch_reduce(const emb_table* t, const unsigned* K, const un
   TableView v = t->view();
   const int threads = kRedWarps * 32;
   int per_sm = 0;
-  cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, segreduce_adagrad_kernel<TW, G, VW, NCB, U>, threads, 0);
+  const bool all_cols = t->uniform_dim == G * VW * NCB;
+  auto kern = all_cols ? segreduce_adagrad_kernel<TW, G, VW, NCB, U, true>
+                       : segreduce_adagrad_kernel<TW, G, VW, NCB, U, false>;
+  cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, threads, 0);
   long long blocks = ((long long)L.n_chunks + (threads / 32) * P - 1) / ((threads / 32) * P);
   blocks = std::min<long long>(blocks, (long long)std::max(1, per_sm) * sm_count());
   float* pa = (float*)(ws + L.partA);
   float* pb = (float*)(ws + L.partB);
   unsigned* ar = (unsigned*)(ws + L.arow);
   float* zrow = (float*)(ws + L.zero);
-  cudaError_t e = cudaMemsetAsync(zrow, 0, (size_t)L.max_dim * 4, st);
+  cudaError_t e = cudaMemsetAsync(zrow, 0, (size_t)EMB_MAX_DIM * 4, st);
   if (e != cudaSuccess) return e;
   // sub-chunks are handed out in order from a counter: all resident groups
   // then work inside a narrow window of one feature slot, whose grad_out
@@ -949,7 +972,7 @@ static cudaError_t launch_reduce(const emb_table* t, const unsigned* K, const un
   unsigned* work = (unsigned*)(ws + L.work);
   e = cudaMemsetAsync(work, 0, sizeof(unsigned), st);
   if (e != cudaSuccess) return e;
-  segreduce_adagrad_kernel<TW, G, VW, NCB, U><<<(int)std::max(1LL, blocks), threads, 0, st>>>(
+  kern<<<(int)std::max(1LL, blocks), threads, 0, st>>>(
       v, K, V, scale, mean, grad, zrow, n, n_bags, L.n_chunks, pa, pb, ar, lr, eps, work);
   mark_phase(t, 2, st);
   // the fixup reads partial rows four columns per lane
@@ -1091,6 +1114,7 @@ emb_status emb_bwd_adagrad_noalloc(emb_table* table, const int64_t* offsets_d, i
   emb_status rc = check_batch(table, offsets_d, n_bags, keys_d, nnz, pool);
   if (rc != EMB_OK) return rc;
   if (n_bags > 0 && !grad_out_d) return fail(EMB_ERR_INVALID_ARG, "grad_out is NULL");
+  if (((uintptr_t)grad_out_d & 15) != 0) return fail(EMB_ERR_INVALID_ARG, "grad_out must be 16-byte aligned");
   const WsLayout L = ws_layout(table, n_bags, nnz);
   if (L.total > (size_t)EMB_NOALLOC_SCRATCH_BYTES) {
     char buf[192];
@@ -1111,6 +1135,7 @@ emb_status emb_lookup_fwd_record(emb_table* table, const int64_t* offsets_d, int
   emb_status rc = check_batch(table, offsets_d, n_bags, keys_d, nnz, pool);
   if (rc != EMB_OK) return rc;
   if (n_bags > 0 && !out_d) return fail(EMB_ERR_INVALID_ARG, "out is NULL");
+  if (((uintptr_t)out_d & 15) != 0) return fail(EMB_ERR_INVALID_ARG, "out must be 16-byte aligned");
   const WsLayout L = ws_layout(table, n_bags, nnz);
   if (!workspace_d || ws_bytes < L.total) return fail(EMB_ERR_WORKSPACE, "workspace missing or too small");
   if (((uintptr_t)workspace_d & 255) != 0) return fail(EMB_ERR_WORKSPACE, "workspace must be 256-byte aligned");
@@ -1144,6 +1169,7 @@ emb_status emb_bwd_adagrad_recorded(emb_table* table, int64_t n_bags, int64_t nn
       (int)pool != table->rec_pool)
     return fail(EMB_ERR_INVALID_ARG, "no emb_lookup_fwd_record of this batch shape in this workspace");
   if (n_bags > 0 && !grad_out_d) return fail(EMB_ERR_INVALID_ARG, "grad_out is NULL");
+  if (((uintptr_t)grad_out_d & 15) != 0) return fail(EMB_ERR_INVALID_ARG, "grad_out must be 16-byte aligned");
   const WsLayout L = ws_layout(table, n_bags, nnz);
   if (ws_bytes < L.total) return fail(EMB_ERR_WORKSPACE, "workspace missing or too small");
   return run_bwd(table, nullptr, n_bags, nullptr, nnz, pool, grad_out_d, lr, eps, (char*)workspace_d, L,
@@ -1171,6 +1197,7 @@ emb_status emb_bwd_adagrad(emb_table* table, const int64_t* offsets_d, int64_t n
   emb_status rc = check_batch(table, offsets_d, n_bags, keys_d, nnz, pool);
   if (rc != EMB_OK) return rc;
   if (n_bags > 0 && !grad_out_d) return fail(EMB_ERR_INVALID_ARG, "grad_out is NULL");
+  if (((uintptr_t)grad_out_d & 15) != 0) return fail(EMB_ERR_INVALID_ARG, "grad_out must be 16-byte aligned");
   const WsLayout L = ws_layout(table, n_bags, nnz);
   if (!workspace_d || ws_bytes < L.total) return fail(EMB_ERR_WORKSPACE, "workspace missing or too small");
   if (((uintptr_t)workspace_d & 255) != 0) return fail(EMB_ERR_WORKSPACE, "workspace must be 256-byte aligned");

@@ -58,6 +58,13 @@ __device__ __forceinline__ void st16_streaming(float* p, float a, float b, float
   asm volatile("st.global.cs.v4.f32 [%0], {%1,%2,%3,%4};" ::"l"(p), "f"(a), "f"(b), "f"(c), "f"(d) : "memory");
 }
 
+// Eight pooled floats, one whole 32-byte sector, in one streaming store.
+__device__ __forceinline__ void st32_streaming(float* p, const float* v, float s) {
+  asm volatile("st.global.cs.v8.f32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8};" ::"l"(p), "f"(v[0] / s), "f"(v[1] / s),
+               "f"(v[2] / s), "f"(v[3] / s), "f"(v[4] / s), "f"(v[5] / s), "f"(v[6] / s), "f"(v[7] / s)
+               : "memory");
+}
+
 __device__ __forceinline__ int pow2_at_least(int x) {
   int g = 1;
   while (g < x) g <<= 1;
@@ -194,10 +201,16 @@ __global__ void __launch_bounds__(256, 8) fwd_pool_kernel(TableView t, const lon
       for (int c = 0; c < NCB; ++c) {
         const int ce = (c * G + li) * VEC;
         if (ce < D) {
+          // a lane's 8 floats (f16 rows) are one sector: written whole when
+          // aligned, so no sector reaches DRAM half-written
+          if (VEC == 8 && ((uintptr_t)(o + ce) & 31) == 0) {
+            st32_streaming(o + ce, acc[c], den);
+          } else {
 #pragma unroll
-          for (int j = 0; j < VEC; j += 4)
-            st16_streaming(o + ce + j, acc[c][j] / den, acc[c][j + 1] / den, acc[c][j + 2] / den,
-                           acc[c][j + 3] / den);
+            for (int j = 0; j < VEC; j += 4)
+              st16_streaming(o + ce + j, acc[c][j] / den, acc[c][j + 1] / den, acc[c][j + 2] / den,
+                             acc[c][j + 3] / den);
+          }
         }
       }
     }
@@ -278,6 +291,7 @@ extern "C" emb_status emb_lookup_fwd(emb_table* table, const int64_t* offsets_d,
   if (rc != EMB_OK) return rc;
   if (n_bags == 0) return EMB_OK;
   if (!out_d) return fail(EMB_ERR_INVALID_ARG, "out is NULL");
+  if (((uintptr_t)out_d & 15) != 0) return fail(EMB_ERR_INVALID_ARG, "out must be 16-byte aligned");
   cudaStream_t st = (cudaStream_t)stream;
   cudaError_t e = launch_forward(table, (const long long*)offsets_d, n_bags, (const long long*)keys_d, nnz,
                                  pool == EMB_POOL_MEAN, out_d, nullptr, nullptr, nullptr, nullptr, st);

@@ -144,6 +144,19 @@ def test_hot_key_spanning_many_reduce_chunks(wdtype, D):
     check_step(cfg, wl, gs)
 
 
+@pytest.mark.parametrize("wdtype,D", [("f32", 64), ("f16", 128)])
+@pytest.mark.parametrize("pool", ["sum", "mean"])
+def test_reduce_windows_of_distinct_rows(wdtype, D, pool):
+    # 4000 distinct keys, one occurrence each, then a hot key: every 32-position
+    # window of the sorted pairs starts 32 rows (the reduce's crowded-window
+    # path), and chunk edges cut both singleton runs and the hot segment
+    bags = [[[_key(0, b * 40 + j + 1) for j in range(40)]] for b in range(100)]
+    bags += [[[_key(0, 7)] * 300] for _ in range(4)]
+    cfg, wl = _handmade(4096, [D], wdtype, bags, pool)
+    gs = gpu_step(cfg, wl)
+    check_step(cfg, wl, gs)
+
+
 def test_nnz_zero_and_single_bag():
     cfg, wl = _handmade(16, [8], "f32", [[[]]])
     gs = gpu_step(cfg, wl)
@@ -177,6 +190,16 @@ def test_host_side_rejections():
     with pytest.raises(E.EmbError) as ei:
         E.emb_table_create([8], "f32", torch.tensor([3, 3]), capacity=8)
     assert ei.value.name == "EMB_ERR_DUP_KEY"
+    # pooled rows are written, and grad_out rows read, with 16-byte vector
+    # accesses: a pointer 4 bytes past a 16-byte boundary is refused on the host
+    buf = torch.empty(16 + 1, dtype=torch.float32, device="cuda")
+    with pytest.raises(E.EmbError) as ei:
+        E.emb_lookup_fwd(tbl, off, q, "sum", out=buf[1:])
+    assert ei.value.name == "EMB_ERR_INVALID_ARG" and "aligned" in ei.value.message
+    ws = torch.empty(E.emb_bwd_workspace_size(tbl, off.numel() - 1, q.numel()), dtype=torch.uint8, device="cuda")
+    with pytest.raises(E.EmbError) as ei:
+        E.emb_bwd_adagrad(tbl, off, q, "sum", buf[1:], 0.1, 1e-8, ws)
+    assert ei.value.name == "EMB_ERR_INVALID_ARG" and "aligned" in ei.value.message
 
 
 def test_resolve_sentinel_and_absent_keys():
