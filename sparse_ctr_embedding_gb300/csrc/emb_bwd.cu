@@ -47,7 +47,7 @@ cudaError_t launch_forward(const emb_table* t, const long long* offsets, long lo
                            long long nnz, int mean, float* out, unsigned* K, unsigned* V, float* scale,
                            unsigned long long* work, cudaStream_t st);
 
-constexpr int kChunk = 512;                      // sorted positions per reduce sub-chunk
+constexpr int kChunk = 256;                      // sorted positions per reduce sub-chunk
 constexpr int kSortWarps = 8;
 constexpr int kSortThreads = kSortWarps * 32;
 constexpr int kSortItems = 16;                   // keys per lane per tile
@@ -633,7 +633,7 @@ __device__ __forceinline__ void fma_vw(float* acc, float w, const float* g) {
 
 // kAllCols: every lane column is inside every row (one dim, equal to G x VW x NCB).
 template <typename TW, int G, int VW, int NCB, int U, bool kAllCols>
-__global__ void __launch_bounds__(kRedWarps * 32, 8) segreduce_adagrad_kernel(
+__global__ void __launch_bounds__(kRedWarps * 32, 10) segreduce_adagrad_kernel(
     TableView t, const unsigned* __restrict__ K, const unsigned* __restrict__ V, const float* __restrict__ scale,
     int mean, const float* __restrict__ grad, const float* __restrict__ zrow, unsigned n, unsigned n_bags,
     unsigned n_chunks, float* __restrict__ partA, float* __restrict__ partB, unsigned* __restrict__ arow, float lr,
@@ -830,8 +830,16 @@ __global__ void __launch_bounds__(256) fixup_kernel(TableView t, const unsigned*
   for (unsigned c = (blockIdx.x * blockDim.x + threadIdx.x) >> 5; c < n_chunks; c += nwarps) {
     const unsigned row = arow[c];
     if (row >= t.n_rows || c + 1 >= n_chunks) continue;
-    // last chunk whose first position still holds this row (K is sorted)
-    unsigned lo = c + 1, hi = n_chunks - 1;
+    // last chunk whose first position still holds this row (K is sorted; the
+    // row continues into chunk c + 1 because chunk c left a head partial).
+    // Exponential search from c + 1: most such rows end in the next chunk.
+    unsigned lo = c + 1, step = 1, probe_c = c + 2;
+    while (probe_c < n_chunks && K[(size_t)probe_c * kChunk] == row) {
+      lo = probe_c;
+      step <<= 1;
+      probe_c = lo + step;
+    }
+    unsigned hi = min(probe_c, n_chunks) - 1;  // K[lo * kChunk] == row, answer in [lo, hi]
     while (lo < hi) {
       const unsigned mid = lo + (hi - lo + 1) / 2;
       if (K[(size_t)mid * kChunk] == row) lo = mid; else hi = mid - 1;
