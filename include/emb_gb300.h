@@ -89,6 +89,12 @@ typedef enum { EMB_POOL_SUM = 0, EMB_POOL_MEAN = 1 } emb_pool;
 #define EMB_MAX_NNZ 2147483647LL   /* per call */
 #define EMB_MAX_BAGS 2147483647LL  /* per call */
 
+/* Digit width of the backward's stable radix sort of (row, bag) pairs: a
+ * table of n keys sorts in ceil(bits(n) / EMB_SORT_DIGIT_BITS) passes, each
+ * one digit-count, three scan and one scatter launch (no counterpart in the
+ * pages; stated so callers can count the kernels a step launches). */
+#define EMB_SORT_DIGIT_BITS 7
+
 typedef struct {
   int32_t n_slots;         /* feature tables merged into the unified table, 1..65535 */
   const int32_t* slot_dim; /* host [n_slots]: embedding dim of each slot */

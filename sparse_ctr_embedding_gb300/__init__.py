@@ -22,7 +22,7 @@ __all__ = [
     "EmbError", "LibraryNotBuilt", "Table", "lib", "declared_symbols",
     "emb_table_create", "emb_table_destroy", "emb_table_get_stats", "emb_table_plan",
     "emb_lookup_fwd", "emb_lookup_fwd_record", "emb_bwd_adagrad_recorded", "emb_bwd_workspace_size", "emb_bwd_adagrad", "emb_bwd_adagrad_noalloc",
-    "emb_bwd_unique_keys", "emb_bwd_phase_events", "EMB_NOALLOC_SCRATCH_BYTES", "BWD_PHASES",
+    "emb_bwd_unique_keys", "emb_bwd_phase_events", "EMB_NOALLOC_SCRATCH_BYTES", "EMB_SORT_DIGIT_BITS", "BWD_PHASES",
     "emb_resolve", "emb_table_export", "emb_table_export_rows", "emb_table_slots", "emb_check_device_flag",
     "emb_status_string", "emb_last_error",
     "EMB_FLAG_PROBE_BOUND", "EMB_FLAG_BAD_OFFSETS", "EMB_FLAG_SLOT_MISMATCH", "EMB_FLAG_BAD_ROW",
@@ -34,6 +34,7 @@ STATUS = {0: "EMB_OK", 1: "EMB_ERR_INVALID_ARG", 2: "EMB_ERR_CUDA", 3: "EMB_ERR_
           8: "EMB_ERR_DEVICE_FLAG", 9: "EMB_ERR_UNSUPPORTED"}
 EMB_FLAG_PROBE_BOUND, EMB_FLAG_BAD_OFFSETS, EMB_FLAG_SLOT_MISMATCH, EMB_FLAG_BAD_ROW = 1, 2, 4, 8
 EMB_NOALLOC_SCRATCH_BYTES = 64 << 20
+EMB_SORT_DIGIT_BITS = 7
 BWD_PHASES = ("expand", "sort", "reduce", "fixup")
 _DTYPE = {"f32": 0, "f16": 1}
 _POOL = {"sum": 0, "mean": 1}

@@ -52,7 +52,7 @@ constexpr int kSortWarps = 8;
 constexpr int kSortThreads = kSortWarps * 32;
 constexpr int kSortItems = 16;                   // keys per lane per tile
 constexpr int kSortTile = kSortThreads * kSortItems;
-constexpr int kRadixBits = 9;                    // 27-bit rows (100M) sort in 3 passes
+constexpr int kRadixBits = EMB_SORT_DIGIT_BITS;  // 7: 27-bit rows (100M) sort in 4 passes
 constexpr int kDigits = 1 << kRadixBits;
 constexpr int kScanThreads = 256;
 constexpr int kScanItems = 16;

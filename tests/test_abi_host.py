@@ -25,6 +25,18 @@ def test_library_exports_every_declared_symbol():
     assert E.emb_status_string(0) == "ok"
 
 
+def test_binding_constants_match_the_header():
+    import re
+    text = open(E.HEADER).read()
+    defs = {m.group(1): m.group(2) for m in re.finditer(r"^#define (EMB_\w+)\s+\(?([0-9]+u?(?: << [0-9]+)?)\)?", text, re.M)}
+    val = lambda v: eval(v.replace("u", ""))
+    assert val(defs["EMB_NOALLOC_SCRATCH_BYTES"]) == E.EMB_NOALLOC_SCRATCH_BYTES
+    assert val(defs["EMB_SORT_DIGIT_BITS"]) == E.EMB_SORT_DIGIT_BITS
+    assert val(defs["EMB_BWD_PHASES"]) == len(E.BWD_PHASES)
+    for f in ["EMB_FLAG_PROBE_BOUND", "EMB_FLAG_BAD_OFFSETS", "EMB_FLAG_SLOT_MISMATCH", "EMB_FLAG_BAD_ROW"]:
+        assert val(defs[f]) == getattr(E, f)
+
+
 @pytest.mark.parametrize("cfg", [W.config(1), W.scaled(W.config(2), 100, 1), W.scaled(W.config(4), 200, 1),
                                  W.scaled(W.config(5), 1000, 1)], ids=lambda c: c.name)
 def test_host_layout_matches_oracle_bit_exact(cfg):
