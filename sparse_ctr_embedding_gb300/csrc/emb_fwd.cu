@@ -58,10 +58,10 @@ __device__ __forceinline__ void st16_streaming(float* p, float a, float b, float
   asm volatile("st.global.cs.v4.f32 [%0], {%1,%2,%3,%4};" ::"l"(p), "f"(a), "f"(b), "f"(c), "f"(d) : "memory");
 }
 
-// Eight pooled floats, one whole 32-byte sector, in one streaming store.
+// Eight pooled floats times s, one whole 32-byte sector, in one streaming store.
 __device__ __forceinline__ void st32_streaming(float* p, const float* v, float s) {
-  asm volatile("st.global.cs.v8.f32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8};" ::"l"(p), "f"(v[0] / s), "f"(v[1] / s),
-               "f"(v[2] / s), "f"(v[3] / s), "f"(v[4] / s), "f"(v[5] / s), "f"(v[6] / s), "f"(v[7] / s)
+  asm volatile("st.global.cs.v8.f32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8};" ::"l"(p), "f"(v[0] * s), "f"(v[1] * s),
+               "f"(v[2] * s), "f"(v[3] * s), "f"(v[4] * s), "f"(v[5] * s), "f"(v[6] * s), "f"(v[7] * s)
                : "memory");
 }
 
@@ -96,6 +96,7 @@ __global__ void __launch_bounds__(256, 8) fwd_pool_kernel(TableView t, const lon
   const unsigned tmask = TEAM == 32 ? 0xffffffffu : (((1u << TEAM) - 1u) << (team * TEAM));
   const long long nteams = (((long long)gridDim.x * blockDim.x) >> 5) * BPW;
   const TW* W = static_cast<const TW*>(t.W);
+  const int G0 = t.uniform_dim ? min(TEAM, pow2_at_least(t.uniform_dim / VEC)) : 0;  // lanes per key, one dim
   // bags: a static grid-stride order, or batches of kBagBatch consecutive bags
   // taken in order from a counter (balances warps over bags of very
   // different lengths)
@@ -129,7 +130,7 @@ __global__ void __launch_bounds__(256, 8) fwd_pool_kernel(TableView t, const lon
       ebase = si.elem_base;
       rbase = si.row_base;
     }
-    const int G = min(TEAM, pow2_at_least(D / VEC));  // lanes per key
+    const int G = t.uniform_dim ? G0 : min(TEAM, pow2_at_least(D / VEC));  // lanes per key
     const int P = TEAM / G;                           // keys pooled side by side
     const int sub = tl / G, li = tl % G;
 
@@ -195,7 +196,9 @@ __global__ void __launch_bounds__(256, 8) fwd_pool_kernel(TableView t, const lon
     if (kRecord && mean && tl == 0) rec.scale[bag] = end > start ? 1.0f / (float)(end - start) : 0.f;
     if (sub == 0) {
       const long long L = end - start;
-      const float den = (mean && L > 0) ? (float)L : 1.f;  // mean over L counting misses; L = 0 gives 0
+      // mean over L counting misses, as one reciprocal times each sum (within
+      // one rounding of the quotient); L = 0 gives 0
+      const float inv = (mean && L > 0) ? 1.f / (float)L : 1.f;
       float* o = out + b * t.sum_dims + col;
 #pragma unroll
       for (int c = 0; c < NCB; ++c) {
@@ -204,12 +207,12 @@ __global__ void __launch_bounds__(256, 8) fwd_pool_kernel(TableView t, const lon
           // a lane's 8 floats (f16 rows) are one sector: written whole when
           // aligned, so no sector reaches DRAM half-written
           if (VEC == 8 && ((uintptr_t)(o + ce) & 31) == 0) {
-            st32_streaming(o + ce, acc[c], den);
+            st32_streaming(o + ce, acc[c], inv);
           } else {
 #pragma unroll
             for (int j = 0; j < VEC; j += 4)
-              st16_streaming(o + ce + j, acc[c][j] / den, acc[c][j + 1] / den, acc[c][j + 2] / den,
-                             acc[c][j + 3] / den);
+              st16_streaming(o + ce + j, acc[c][j] * inv, acc[c][j + 1] * inv, acc[c][j + 2] * inv,
+                             acc[c][j + 3] * inv);
           }
         }
       }
