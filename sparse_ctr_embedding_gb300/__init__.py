@@ -78,7 +78,7 @@ def lib():
     global _lib
     if _lib is None:
         if not os.path.exists(LIB_PATH):
-            raise LibraryNotBuilt(f"{LIB_PATH} is missing: run `python -c 'import __graft_entry__ as g; g.build()'`")
+            raise LibraryNotBuilt(f"{LIB_PATH} is missing: run `python -c 'import sparse_ctr_embedding_gb300 as E; E.build()'`")
         L = ctypes.CDLL(LIB_PATH)
         sig = {
             "emb_table_create": [ctypes.POINTER(_Desc), _vp, _i64, _vp, _vp, _vp, ctypes.POINTER(_vp)],
