@@ -565,7 +565,7 @@ __device__ __forceinline__ void prefetch_row(const TableView& t, const RowGeo& g
   for (int o = 0; o < g.D * 4; o += 128) prefetch_l2(a + o);
 }
 
-// VW consecutive floats of grad_out: one 16- or 32-byte read-only load.
+// VW consecutive floats of grad_out: one 16-byte read-only load.
 template <int VW>
 struct GradVec;
 template <>
@@ -574,15 +574,6 @@ struct GradVec<4> {
   __device__ __forceinline__ void load(const float* p) {
     const float4 x = __ldg(reinterpret_cast<const float4*>(p));
     v[0] = x.x; v[1] = x.y; v[2] = x.z; v[3] = x.w;
-  }
-};
-template <>
-struct GradVec<8> {
-  float v[8];
-  __device__ __forceinline__ void load(const float* p) {
-    asm("ld.global.nc.v8.f32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%8];"
-        : "=f"(v[0]), "=f"(v[1]), "=f"(v[2]), "=f"(v[3]), "=f"(v[4]), "=f"(v[5]), "=f"(v[6]), "=f"(v[7])
-        : "l"(p));
   }
 };
 
