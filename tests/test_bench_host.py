@@ -1,0 +1,36 @@
+"""bench.py's host-side bookkeeping, without a GPU: the stored ncu traffic is
+reported only for the CUDA sources it was measured on, and the kernel count
+per step follows the sort's digit width."""
+import json
+import os
+import sys
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+sys.path.insert(0, ROOT)
+
+import bench  # noqa: E402
+import sparse_ctr_embedding_gb300 as E  # noqa: E402
+
+
+def test_stored_traffic_requires_matching_sources(monkeypatch):
+    with open(os.path.join(ROOT, "profiles", "dram_traffic.json")) as f:
+        rec = json.load(f)
+    wl, per = next(iter(rec["workloads"].items()))
+    kernel, value = next(iter(per.items()))
+    monkeypatch.setattr(bench, "kernel_fingerprint", lambda: rec["fingerprint"])
+    assert bench.stored_traffic(wl, kernel) == value
+    assert bench.stored_traffic(wl, "no_such_kernel") is None
+    monkeypatch.setattr(bench, "kernel_fingerprint", lambda: "0" * 64)
+    assert bench.stored_traffic(wl, kernel) is None
+
+
+def test_fingerprint_is_stable():
+    fp = bench.kernel_fingerprint()
+    assert len(fp) == 64 and fp == bench.kernel_fingerprint()
+
+
+def test_launches_per_step_follow_the_digit_width():
+    # header + recording forward, 5 launches per radix pass, reduce, fixup
+    assert bench.launches_per_step(100_000_000, E.EMB_SORT_DIGIT_BITS) == 2 + 4 * 5 + 2   # 27 bits, 4 passes
+    assert bench.launches_per_step(65_536, E.EMB_SORT_DIGIT_BITS) == 2 + 3 * 5 + 2       # 17 bits, 3 passes
+    assert bench.launches_per_step(100, 7) == 2 + 1 * 5 + 2
