@@ -394,9 +394,9 @@ def run_ours(args):
         off_h = offsets.cpu().pin_memory()
         q_h = qkeys.cpu().pin_memory()
         g_h = grad.cpu().pin_memory()
-        outs_h = [torch.empty(out.shape, dtype=out.dtype).pin_memory() for _ in range(2)]
+        out_h = torch.empty(out.shape, dtype=out.dtype).pin_memory()  # downloads are serialised on one stream
         h2d = off_h.numel() * 8 + q_h.numel() * 8 + g_h.numel() * 4
-        d2h = outs_h[0].numel() * 4
+        d2h = out_h.numel() * 4
         bufs = [(offsets, qkeys, grad, out),
                 (torch.empty_like(offsets), torch.empty_like(qkeys), torch.empty_like(grad), torch.empty_like(out))]
         up, down = torch.cuda.Stream(device=dev), torch.cuda.Stream(device=dev)
@@ -432,7 +432,7 @@ def run_ours(args):
                 done[i % 2].record(stream)
                 with torch.cuda.stream(down):
                     down.wait_event(done[i % 2])
-                    outs_h[i % 2].copy_(ob, non_blocking=True)
+                    out_h.copy_(ob, non_blocking=True)
                     freed[i % 2].record(down)
             stream.wait_event(freed[(n_steps - 1) % 2])
             b.record(stream)
