@@ -13,6 +13,7 @@ Prints ONE JSON line (rank 0).  --impl reference times the CPU oracle instead.
 from __future__ import annotations
 
 import argparse
+import dataclasses
 import json
 import math
 import os
@@ -35,6 +36,8 @@ def parse():
     ap.add_argument("--steps", type=int, default=20)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--config", type=int, default=5, help="workload 1..5")
+    ap.add_argument("--wdtype", default=None, choices=["f32", "f16", "f16m"],
+                    help="weight storage instead of the workload's own (f16m: f32 master rows + f16 copy)")
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--vocab-div", type=int, default=1, help="shrink keys per slot (profiling a small case)")
     ap.add_argument("--batch-div", type=int, default=1, help="shrink the batch (profiling a small case)")
@@ -290,6 +293,8 @@ def run_ours(args):
     cfg = W.config(args.config)
     if args.vocab_div > 1 or args.batch_div > 1:
         cfg = W.scaled(cfg, args.vocab_div, args.batch_div)
+    if args.wdtype and args.wdtype != cfg.wdtype:
+        cfg = dataclasses.replace(cfg, wdtype=args.wdtype, name=f"{cfg.name}/{args.wdtype}")
     stream = torch.cuda.current_stream()
 
     # ---- workload (generated on the device, keys copied to the host for the table build)
@@ -315,7 +320,7 @@ def run_ours(args):
     wsb = torch.empty(E.emb_bwd_workspace_size(tbl, n_bags, nnz), dtype=torch.uint8, device=dev)
 
     # ---- algorithmic bytes of one step (the bytes the method must move)
-    wsz = 2 if cfg.wdtype == "f16" else 4
+    wsz = 2 if cfg.wdtype in ("f16", "f16m") else 4   # bytes of a row element the forward gathers
     _, rows = E.emb_resolve(tbl, qkeys)
     hit = rows >= 0
     dims_t = torch.tensor(cfg.dims, dtype=torch.int64, device=dev)
@@ -338,7 +343,9 @@ def run_ours(args):
     E.emb_bwd_unique_keys(tbl, wsb, uk, nu)
     n_unique = int(nu.item())
     d_u = dims_t[uk[:n_unique] >> 48]
-    rmw_bytes = int(d_u.sum()) * (2 * wsz + 8)
+    # per updated element: weights and accumulator read and written; a master-copy
+    # table updates the f32 master and writes the element's f16 copy
+    rmw_bytes = int(d_u.sum()) * (2 * 4 + 8 + 2 if cfg.wdtype == "f16m" else 2 * wsz + 8)
     del uk, d_u
     # the recording forward resolved every key once; the backward reads grad_out
     # and read-modify-writes the hit rows (the cached row ids are workspace)
@@ -357,7 +364,8 @@ def run_ours(args):
     clocks = Clocks(local)
     clocks.start()
     K = args.steps
-    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(2 + len(E.BWD_PHASES))] for _ in range(K)]
+    # per step: start, forward done, the backward's phases, backward call done
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3 + len(E.BWD_PHASES))] for _ in range(K)]
     for e in ev:                      # torch creates the CUDA event on first record
         for x in e:
             x.record(stream)
@@ -366,8 +374,9 @@ def run_ours(args):
         ev[k][0].record(stream)
         E.emb_lookup_fwd_record(tbl, offsets, qkeys, cfg.pool, wsb, out=out)
         ev[k][1].record(stream)
-        E.emb_bwd_phase_events(tbl, ev[k][2:])
+        E.emb_bwd_phase_events(tbl, ev[k][2:-1])
         E.emb_bwd_adagrad_recorded(tbl, n_bags, nnz, cfg.pool, grad, cfg.lr, cfg.eps, wsb)
+        ev[k][-1].record(stream)
     torch.cuda.synchronize()
     barrier(ws)
     clk = clocks.stop()
@@ -383,6 +392,8 @@ def run_ours(args):
     kernel_ms = {"fwd_pool_kernel": fwd_ms,
                  "radix sort (count + scan + scatter kernels)": phase_ms["sort"],
                  "segreduce_adagrad_kernel": phase_ms["reduce"], "fixup_kernel": phase_ms["fixup"]}
+    if cfg.wdtype == "f16m":
+        kernel_ms["refresh_half_kernel"] = statistics.mean(e[-2].elapsed_time(e[-1]) for e in ev)
 
     # ---- end to end through the C ABI: every step's CSR batch and grad_out are
     # copied in from pinned host memory and its pooled output copied back.  The
@@ -491,7 +502,8 @@ def run_ours(args):
         "fwd_roofline": {"achieved": fwd_gbs, "frac": fwd_gbs / peak, "algorithmic_bytes": fwd_bytes},
         "bwd_roofline": {"achieved": bwd_gbs, "frac": bwd_gbs / peak, "algorithmic_bytes": bwd_bytes},
         "cpu_baseline": cpu, "e2e": e2e,
-        "gpu_launches": K * launches_per_step(st["n_keys"], E.EMB_SORT_DIGIT_BITS),
+        "gpu_launches": K * (launches_per_step(st["n_keys"], E.EMB_SORT_DIGIT_BITS)
+                             + (1 if cfg.wdtype == "f16m" else 0)),   # + the f16 copy refresh
         "clocks": clk, "device_flags": flags,
         "setup_s": {"generate": t_gen, "table_create": t_create},
     }

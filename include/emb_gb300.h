@@ -74,7 +74,17 @@ typedef enum {
   EMB_ERR_UNSUPPORTED = 9   /* a size beyond this library's stated limits */
 } emb_status;
 
-typedef enum { EMB_F32 = 0, EMB_F16 = 1 } emb_dtype; /* weight storage; accumulator is always f32 */
+/* Weight storage; the accumulator is always f32.
+ *   EMB_F32, EMB_F16: one copy of every row, read by the forward and updated
+ *     in place (f16 rows are updated in f32 and rounded to nearest-even).
+ *   EMB_F16_MASTER: mixed precision as the JD article describes it (3.2.3:
+ *     rows stored and used in FP16, an FP32 copy of the weights kept for the
+ *     update): an f32 master row, which the update works on and which is what
+ *     create takes and export returns, and an f16 copy of it, which the
+ *     forward reads.  After each update the f16 copy of every updated row is
+ *     its master rounded to nearest-even.  10 bytes per element with the
+ *     accumulator. */
+typedef enum { EMB_F32 = 0, EMB_F16 = 1, EMB_F16_MASTER = 2 } emb_dtype;
 typedef enum { EMB_POOL_SUM = 0, EMB_POOL_MEAN = 1 } emb_pool;
 
 /* Device flag bits reported by emb_check_device_flag. */
@@ -128,8 +138,9 @@ typedef struct {
  *            by one in this order with linear probing from fmix64(key) mod
  *            capacity, so the layout is a pure function of this array.
  *   values   host or device, ragged rows in keys-array order: key i's row has
- *            dim(slot(key_i)) elements of wdtype (float or IEEE half).  NULL
- *            fills the weights with zeros.
+ *            dim(slot(key_i)) elements of wdtype (float, IEEE half, or float
+ *            for EMB_F16_MASTER: the master rows, whose f16 copy is made
+ *            here).  NULL fills the weights with zeros.
  *   acc      host or device float32, same element layout as values; NULL fills
  *            with desc->acc_init.
  *   stream   stream for the uploads; the call synchronises it before return.
@@ -282,7 +293,8 @@ EMB_API emb_status emb_resolve(const emb_table* table, const int64_t* keys_d, in
 
 /*
  * emb_table_export -- checkpoint: copy keys, weights and accumulators back in
- * keys-array order (same layouts as emb_table_create's inputs).  Destinations
+ * keys-array order (same layouts as emb_table_create's inputs; the f32 master
+ * rows for EMB_F16_MASTER).  Destinations
  * are host or device; any may be NULL.  Synchronises `stream`.  Creating a
  * table from the exported arrays resumes it exactly.
  */

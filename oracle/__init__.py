@@ -84,6 +84,13 @@ def f32_to_f16_bits(x: np.ndarray) -> np.ndarray:
     return out
 
 
+def f16_copy(master: np.ndarray) -> np.ndarray:
+    """The rows the forward reads from a master-copy table (JD article 3.2.3:
+    FP16 storage and compute, an FP32 copy of the weights for the update):
+    each f32 master element rounded to nearest-even, as float16."""
+    return f32_to_f16_bits(master).view(np.float16)
+
+
 WDTYPE = {"f32": 0, "f16": 1}
 POOL = {"sum": 0, "mean": 1}
 

@@ -36,7 +36,7 @@ EMB_FLAG_PROBE_BOUND, EMB_FLAG_BAD_OFFSETS, EMB_FLAG_SLOT_MISMATCH, EMB_FLAG_BAD
 EMB_NOALLOC_SCRATCH_BYTES = 64 << 20
 EMB_SORT_DIGIT_BITS = 7
 BWD_PHASES = ("expand", "sort", "reduce", "fixup")
-_DTYPE = {"f32": 0, "f16": 1}
+_DTYPE = {"f32": 0, "f16": 1, "f16m": 2}   # f16m: f32 master rows + the f16 copy the forward reads
 _POOL = {"sum": 0, "mean": 1}
 
 

@@ -887,6 +887,45 @@ __global__ void __launch_bounds__(256) fixup_kernel(TableView t, const unsigned*
   }
 }
 
+// ------------------------------------------------------------------ 5. f16 copy of master-copy tables
+//
+// Mixed precision as the JD article describes it (3.2.3): the update works on
+// the f32 master rows (the f32 reduce above, with W the master); the forward
+// reads their f16 copy, refreshed here for every row the step updated (the
+// run heads of the sorted pairs), rounded to nearest-even.  One warp per 32
+// sorted positions copies each row that starts among them, four elements
+// per lane.
+__global__ void __launch_bounds__(256) refresh_half_kernel(TableView t, const unsigned* __restrict__ K, unsigned n,
+                                                           __half* __restrict__ W16) {
+  const int lane = threadIdx.x & 31;
+  const unsigned nw = (gridDim.x * blockDim.x) >> 5;
+  const unsigned miss = t.n_rows;
+  const float* M = static_cast<const float*>(t.W);
+  for (unsigned w = (blockIdx.x * blockDim.x + threadIdx.x) >> 5; (size_t)w * 32 < n; w += nw) {
+    const unsigned i = w * 32 + lane;
+    const unsigned k = i < n ? K[i] : miss;
+    const unsigned kp = (i < n && i > 0) ? K[i - 1] : kNoRow;
+    unsigned heads = __ballot_sync(0xffffffffu, i < n && k < miss && k != kp);
+    while (heads) {
+      const int j = __ffs(heads) - 1;
+      heads &= heads - 1;
+      const unsigned row = __shfl_sync(0xffffffffu, k, j);
+      int D, col;
+      long long e0;
+      row_geom(t, row, D, col, e0);
+      for (int c = lane * 4; c < D; c += 128) {  // D is a multiple of 8 for tables with f16 rows
+        const float4 m = *reinterpret_cast<const float4*>(M + e0 + c);
+        const __half2 a = __floats2half2_rn(m.x, m.y);
+        const __half2 b = __floats2half2_rn(m.z, m.w);
+        uint2 x;
+        x.x = *reinterpret_cast<const unsigned*>(&a);
+        x.y = *reinterpret_cast<const unsigned*>(&b);
+        *reinterpret_cast<uint2*>(W16 + e0 + c) = x;
+      }
+    }
+  }
+}
+
 // ------------------------------------------------------------------ unique-key export
 
 __global__ void __launch_bounds__(kScanThreads) head_count_kernel(const unsigned* __restrict__ K, size_t n,
@@ -1077,6 +1116,12 @@ static emb_status run_bwd(emb_table* table, const int64_t* offsets_d, int64_t n_
                       ? dispatch_reduce<__half>(table, ki, vi, scale, mean, grad_out_d, n, (unsigned)n_bags, L, ws, lr, eps, st)
                       : dispatch_reduce<float>(table, ki, vi, scale, mean, grad_out_d, n, (unsigned)n_bags, L, ws, lr, eps, st);
   if (e != cudaSuccess) return cuda_fail(e, "segmented reduce launch");
+  if (table->W16_d && n > 0) {  // master-copy table: the forward's f16 rows follow the updated masters
+    const long long blocks = std::min<long long>(((long long)n + 255) / 256, resident_blocks(256));
+    refresh_half_kernel<<<(int)std::max(1LL, blocks), 256, 0, st>>>(v, ki, n, (__half*)table->W16_d);
+    e = cudaGetLastError();
+    if (e != cudaSuccess) return cuda_fail(e, "f16 copy refresh launch");
+  }
   return EMB_OK;
 }
 

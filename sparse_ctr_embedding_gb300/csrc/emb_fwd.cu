@@ -236,7 +236,7 @@ static cudaError_t launch_fwd(const emb_table* t, const long long* offsets, long
   const int ncb = (max_vecs + team - 1) / team;  // column blocks per lane
   const int threads = 256;
   const long long want = std::max(1LL, (n_bags * team + threads - 1) / threads);
-  TableView v = t->view();
+  TableView v = t->fwd_view();
   // grid: one wave of resident blocks, grid-stride over bags
 #define EMB_FWD(TM, NC, UU)                                                                                 \
   do {                                                                                                      \
@@ -267,7 +267,7 @@ cudaError_t launch_forward(const emb_table* t, const long long* offsets, long lo
                            unsigned long long* work, cudaStream_t st) {
   const Record rec{K, V, scale, work};
   const bool record = K != nullptr;
-  if (t->st.wdtype == EMB_F16)
+  if (t->fwd_half())
     return record ? launch_fwd<__half, true>(t, offsets, n_bags, keys, nnz, mean, out, rec, st)
                   : launch_fwd<__half, false>(t, offsets, n_bags, keys, nnz, mean, out, rec, st);
   return record ? launch_fwd<float, true>(t, offsets, n_bags, keys, nnz, mean, out, rec, st)

@@ -9,6 +9,8 @@
 //                            slot are contiguous (slot-major), so a row's
 //                            first element is elem_base[s] + (row - row_base[s]) * dim[s].
 //   ACC     f32[n_elems]     Adagrad accumulators, same layout as W.
+//   W16     f16[n_elems]     EMB_F16_MASTER tables only: the f16 copy of W
+//                            (then the f32 master) that the forward reads.
 //   row_key int64[n_rows]    key of each internal row.
 //   int_to_ext / ext_to_int  u32[n_rows] row-order permutations.
 //   flags   u32              EMB_FLAG_* bits raised by kernels.
@@ -135,7 +137,8 @@ struct emb_table {
   std::vector<emb::SlotInfo> sinfo_h;
   emb::Slot* slots_d = nullptr;
   emb::SlotInfo* sinfo_d = nullptr;
-  void* W_d = nullptr;
+  void* W_d = nullptr;      // weights (the f32 master for EMB_F16_MASTER tables)
+  void* W16_d = nullptr;    // EMB_F16_MASTER tables: the f16 copy the forward reads
   float* ACC_d = nullptr;
   long long* row_key_d = nullptr;
   unsigned int* int_to_ext_d = nullptr;
@@ -168,6 +171,14 @@ struct emb_table {
     v.flags = flags_d;
     return v;
   }
+  // The view the forward gathers from: the f16 copy of a master-copy table.
+  emb::TableView fwd_view() const {
+    emb::TableView v = view();
+    if (W16_d) v.W = W16_d;
+    return v;
+  }
+  // Element type the forward reads.
+  bool fwd_half() const { return st.wdtype == EMB_F16 || st.wdtype == EMB_F16_MASTER; }
 };
 
 namespace emb {

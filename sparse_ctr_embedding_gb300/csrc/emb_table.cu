@@ -60,7 +60,8 @@ static emb_status build_plan(const emb_table_desc* d, const int64_t* keys, int64
   if (n > EMB_MAX_KEYS) return fail(EMB_ERR_UNSUPPORTED, "n_keys exceeds EMB_MAX_KEYS");
   if (d->n_slots < 1 || d->n_slots > 65535 || !d->slot_dim)
     return fail(EMB_ERR_INVALID_ARG, "n_slots must be in [1, 65535] with slot_dim given");
-  if (d->wdtype != EMB_F32 && d->wdtype != EMB_F16) return fail(EMB_ERR_INVALID_ARG, "bad wdtype");
+  if (d->wdtype != EMB_F32 && d->wdtype != EMB_F16 && d->wdtype != EMB_F16_MASTER)
+    return fail(EMB_ERR_INVALID_ARG, "bad wdtype");
   const int vec = d->wdtype == EMB_F32 ? 4 : 8;
   P.n_slots = d->n_slots;
   P.dims.assign(d->slot_dim, d->slot_dim + d->n_slots);
@@ -222,6 +223,12 @@ __global__ void permute_rows_kernel(TableView t, const unsigned* ext_to_int, con
   }
 }
 
+// The f16 copy of a master-copy table: every element rounded to nearest-even.
+__global__ void half_copy_kernel(const float* __restrict__ w, __half* __restrict__ h, long long n) {
+  for (long long i = blockIdx.x * (long long)blockDim.x + threadIdx.x; i < n; i += (long long)gridDim.x * blockDim.x)
+    h[i] = __float2half_rn(w[i]);
+}
+
 __global__ void fill_f32_kernel(float* p, long long n, float v) {
   long long i = blockIdx.x * (long long)blockDim.x + threadIdx.x;
   for (; i < n; i += (long long)gridDim.x * blockDim.x) p[i] = v;
@@ -379,6 +386,7 @@ static void free_table(emb_table* t) {
   cudaFree(t->slots_d);
   cudaFree(t->sinfo_d);
   cudaFree(t->W_d);
+  cudaFree(t->W16_d);
   cudaFree(t->ACC_d);
   cudaFree(t->row_key_d);
   cudaFree(t->int_to_ext_d);
@@ -479,6 +487,14 @@ emb_status emb_table_create(const emb_table_desc* desc, const int64_t* keys_h, i
       if ((r = move_rows(t, values, t->W_d, esz, true, st)) != EMB_OK) return r;
     } else {
       EMB_CUDA(cudaMemsetAsync(t->W_d, 0, ne * esz, st));
+    }
+    if (P.wdtype == EMB_F16_MASTER) {  // W holds the f32 master; the forward reads its f16 copy
+      EMB_CUDA(cudaMalloc(&t->W16_d, ne * 2));
+      bytes += ne * 2;
+      t->st.device_bytes = bytes;
+      half_copy_kernel<<<grid_for((long long)ne, 256), 256, 0, st>>>((const float*)t->W_d, (__half*)t->W16_d,
+                                                                     (long long)ne);
+      EMB_CUDA(cudaGetLastError());
     }
     if (acc) {
       if ((r = move_rows(t, acc, t->ACC_d, 4, true, st)) != EMB_OK) return r;

@@ -86,3 +86,15 @@ def test_plan_stats_count_probes():
     assert st["n_keys"] == 40 and (sk != -1).sum() == 40
     assert st["sum_probe"] >= 40 and st["max_probe"] >= 1
     assert sorted(sr[sr >= 0].tolist()) == list(range(40))
+
+
+def test_master_copy_tables_plan_like_f16_tables():
+    cfg = W.scaled(W.config(5), 2000, 1)
+    keys = W.table_keys(cfg).numpy()
+    st16, sk16, sr16 = E.emb_table_plan(cfg.dims, "f16", keys, cfg.capacity, layout=True)
+    stm, skm, srm = E.emb_table_plan(cfg.dims, "f16m", keys, cfg.capacity, layout=True)
+    assert np.array_equal(sk16, skm) and np.array_equal(sr16, srm)
+    assert stm["wdtype"] == 2 and stm["n_elems"] == st16["n_elems"]
+    with pytest.raises(E.EmbError):
+        E.emb_table_plan([12], "f16m", keys[:4] & ((1 << 48) - 1), 16)     # f16 rows need dims % 8 == 0
+

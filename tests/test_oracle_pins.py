@@ -369,3 +369,16 @@ def test_f16_rounding_matches_numpy():
     mid = ((h.astype(np.float64) + np.nextafter(h, np.float16(np.inf)).astype(np.float64)) / 2).astype(np.float32)
     x = np.concatenate([x, mid])
     assert np.array_equal(oracle.f32_to_f16_bits(x), x.astype(np.float16).view(np.uint16))
+
+
+def test_master_copy_rows_are_the_masters_rounded_to_nearest_even():
+    rng = np.random.default_rng(7)
+    m = np.concatenate([rng.uniform(-0.05, 0.05, 4096).astype(np.float32),
+                        # exact ties between neighbouring halves go to the even one
+                        np.array([1 + 2.0 ** -11, 1 + 3 * 2.0 ** -11, -(1 + 2.0 ** -11), 65504.0, 1e-8],
+                                 dtype=np.float32)])
+    c = oracle.f16_copy(m)
+    assert c.dtype == np.float16
+    assert np.array_equal(c.view(np.uint16), m.astype(np.float16).view(np.uint16))
+    assert c[-5] == np.float16(1.0) and c[-4] == np.float16(1 + 2.0 ** -9) and c[-3] == np.float16(-1.0)
+

@@ -96,7 +96,7 @@ class Config:
     n_slots: int
     vocab: Tuple[int, ...]          # keys per slot, V_s
     dims: Tuple[int, ...]           # embedding dim per slot
-    wdtype: str                     # "f32" | "f16" (accumulator is always f32)
+    wdtype: str                     # "f32" | "f16" | "f16m" (f32 master + f16 copy; accumulator always f32)
     batch: int                      # samples B; bags = B * n_slots
     bag_len: Tuple                  # ("uniform", lo, hi) | ("geometric", p, cap) | ("zipf", s, lo, hi)
     zipf_s: float
