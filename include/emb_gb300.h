@@ -152,14 +152,20 @@ typedef struct {
 EMB_API emb_status emb_table_create(const emb_table_desc* desc, const int64_t* keys_h, int64_t n_keys,
                             const void* values, const float* acc, void* stream, emb_table** out);
 
-/* Free the table and its device memory.  Work queued on it must be complete. */
+/* Free the table and its device memory (the end of a pass, Tencent PCG talk,
+ * "各阶段优化详细介绍").  Work queued on it must be complete. */
 EMB_API emb_status emb_table_destroy(emb_table* table);
 
-/* Host-side statistics of the table (no GPU access). */
+/* Host-side statistics of the table (no GPU access): probe lengths and the
+ * longest cluster of occupied slots.  The JD ads article (4.3) asks that hash
+ * collisions be monitored; this table stores the keys, so two ids never share
+ * a row, and what collisions cost here is longer probes, which these count. */
 EMB_API emb_status emb_table_get_stats(const emb_table* table, emb_table_stats* out);
 
 /*
- * emb_table_plan -- validate desc and keys and compute the statistics the
+ * emb_table_plan -- the preparation step of emb_table_create alone (Tencent
+ * PCG talk, "各阶段优化详细介绍": the table structure is prepared before it
+ * is flashed to the GPU): validate desc and keys and compute the statistics the
  * table would have, on the host only (no CUDA call).  Same errors as
  * emb_table_create apart from OOM/CUDA.  slot_key_h / slot_row_h, if not
  * NULL, receive the host-built layout: int64[capacity] key per slot (-1 =
@@ -185,7 +191,8 @@ EMB_API emb_status emb_table_plan(const emb_table_desc* desc, const int64_t* key
 EMB_API emb_status emb_lookup_fwd(emb_table* table, const int64_t* offsets_d, int64_t n_bags, const int64_t* keys_d,
                           int64_t nnz, emb_pool pool, float* out_d, void* stream);
 
-/* Bytes of device workspace emb_bwd_adagrad needs for this batch shape. */
+/* Bytes of device workspace emb_bwd_adagrad needs for this batch shape (no
+ * counterpart in the pages: the caller owns the backward's scratch memory). */
 EMB_API emb_status emb_bwd_workspace_size(const emb_table* table, int64_t n_bags, int64_t nnz, size_t* bytes);
 
 /*
@@ -235,14 +242,16 @@ EMB_API emb_status emb_bwd_phase_events(emb_table* table, void* const* events, i
  *   - A batch whose workspace (emb_bwd_workspace_size) exceeds
  *     EMB_NOALLOC_SCRATCH_BYTES is rejected with EMB_ERR_UNSUPPORTED before
  *     any work is queued (about 3 million lookups fit at dim 128).
- *   - The first call on a device looks up the array's device address once
- *     (cudaGetSymbolAddress, with that device current); make that first call
- *     before any stream capture.
+ *   - The first call in each CUDA context (per device, and again after a
+ *     cudaDeviceReset) looks up the array's device address with
+ *     cudaGetSymbolAddress, with that device current, and keeps it for that
+ *     context; make that first call before any stream capture.
  *   - Every call on a device shares the one array and leaves its contents
  *     behind.  Calls that can overlap on the GPU (different streams without
  *     ordering, or several threads) race on it and give wrong results: order
  *     them.  No part of the array has to start at zero; each call writes
- *     every region before reading it.
+ *     every region before reading it (with malformed offsets too: positions
+ *     outside every bag are written as absent pairs).
  *   - emb_bwd_unique_keys cannot read this array; use emb_bwd_adagrad with a
  *     workspace when the unique keys are needed.
  * Arguments and errors otherwise as emb_bwd_adagrad.
@@ -276,7 +285,9 @@ EMB_API emb_status emb_bwd_adagrad_recorded(emb_table* table, int64_t n_bags, in
 
 /*
  * emb_bwd_unique_keys -- the deduplicated key set of the last emb_bwd_adagrad
- * that used this workspace.  keys_out_d int64[>= nnz of that call] receives
+ * that used this workspace (Tencent PCG talk, "各阶段优化详细介绍": the
+ * deduplicated keys a group uses are what the pass moves between the GPU table
+ * and the slower tiers; here, the keys the step updated).  keys_out_d int64[>= nnz of that call] receives
  * the unique hit keys (slot-major internal row order); n_unique_d int64[1]
  * receives their count.
  */
@@ -284,7 +295,9 @@ EMB_API emb_status emb_bwd_unique_keys(const emb_table* table, const void* works
                                int64_t* keys_out_d, int64_t* n_unique_d, void* stream);
 
 /*
- * emb_resolve -- the probe alone (parity of slot resolution): for each key,
+ * emb_resolve -- the probe of the unified lookup kernel alone (Tencent PCG
+ * talk, "计算优化": one lookup over the unified table resolves every
+ * feature's keys), for checking slot resolution: for each key,
  * slot_out_d[i] = its slot index in the table or -1, row_out_d[i] = its index
  * in the keys array given to emb_table_create or -1.  Either output may be NULL.
  */
@@ -292,8 +305,9 @@ EMB_API emb_status emb_resolve(const emb_table* table, const int64_t* keys_d, in
                        int64_t* row_out_d, void* stream);
 
 /*
- * emb_table_export -- checkpoint: copy keys, weights and accumulators back in
- * keys-array order (same layouts as emb_table_create's inputs; the f32 master
+ * emb_table_export -- checkpoint (Tencent PCG talk, after "计算优化": a full
+ * model is exported every day and an incremental one every hour): copy keys,
+ * weights and accumulators back in keys-array order (same layouts as emb_table_create's inputs; the f32 master
  * rows for EMB_F16_MASTER).  Destinations
  * are host or device; any may be NULL.  Synchronises `stream`.  Creating a
  * table from the exported arrays resumes it exactly.
@@ -302,8 +316,9 @@ EMB_API emb_status emb_table_export(const emb_table* table, int64_t* keys_out, v
                             void* stream);
 
 /*
- * emb_table_export_rows -- partial checkpoint: the weights and accumulators of
- * selected keys-array rows (ext_rows_d int64[n], indices into the keys array
+ * emb_table_export_rows -- partial checkpoint, the incremental export of the
+ * same passage (the rows a step updated, e.g. from emb_bwd_unique_keys): the
+ * weights and accumulators of selected keys-array rows (ext_rows_d int64[n], indices into the keys array
  * given at creation).  Outputs are device buffers laid out [n, max_dim]: row
  * i's dim(slot) elements first, zero padding after.  Either output may be
  * NULL.  An index outside [0, n_keys) yields a zero row and raises
@@ -313,16 +328,20 @@ EMB_API emb_status emb_table_export_rows(const emb_table* table, const int64_t* 
                                          void* values_out_d, float* acc_out_d, void* stream);
 
 /* Copy the slot layout (key and keys-array index per slot, -1 = empty) to
- * host or device int64[capacity] buffers; either may be NULL.  Synchronises. */
+ * host or device int64[capacity] buffers; either may be NULL.  Synchronises.
+ * No counterpart in the pages: it exposes the prepared layout for checking. */
 EMB_API emb_status emb_table_slots(const emb_table* table, int64_t* slot_key_out, int64_t* slot_row_out, void* stream);
 
 /*
- * emb_check_device_flag -- synchronise `stream`, read and clear the table's
- * device flag word.  Returns EMB_ERR_DEVICE_FLAG if any EMB_FLAG_* bit was set
+ * emb_check_device_flag -- (no counterpart in the pages: kernels report bad
+ * input through a flag word instead of trapping) synchronise `stream`, read
+ * and clear the table's device flag word.  Returns EMB_ERR_DEVICE_FLAG if any EMB_FLAG_* bit was set
  * by a kernel since the last check (flags_out, if not NULL, receives them).
  */
 EMB_API emb_status emb_check_device_flag(emb_table* table, void* stream, uint32_t* flags_out);
 
+/* Human-readable status name, and the calling thread's last error message
+ * (no counterpart in the pages). */
 EMB_API const char* emb_status_string(emb_status s);
 EMB_API const char* emb_last_error(void);
 

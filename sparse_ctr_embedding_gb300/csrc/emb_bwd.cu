@@ -17,15 +17,16 @@
 //               feature slot (one column block of grad_out) at a time.
 //  3. reduce    the sorted positions are cut into chunks of kChunk; one warp
 //               per chunk.  Every run of equal rows inside a chunk ("piece")
-//               is summed in float32, in sorted order (so in occurrence
-//               order: the sort is stable), by a group of G lanes.  A piece
+//               is summed in float32 with TwoSum compensation, in sorted
+//               order (so in occurrence order: the sort is stable), by a
+//               group of G lanes.  A piece
 //               that is a whole segment (all occurrences of its row) applies
 //               Adagrad to the row directly.  A piece cut by a chunk edge
 //               leaves a partial sum: the head piece of a segment in slot A
 //               of its chunk, later pieces in slot B of theirs.
 //  4. fixup     one warp per segment that spans chunks: A + B + B ... in
-//               chunk order (a fixed tree across the warp's lane groups),
-//               then Adagrad.
+//               chunk order (compensated, then a fixed tree across the
+//               warp's lane groups), then Adagrad.
 // No float atomics: every sum has a fixed order, so the step is bitwise
 // reproducible.  The Adagrad arithmetic per element, in float32:
 //   g = G;  acc += g * g;  w -= lr * g / (sqrt(acc) + eps)
@@ -36,6 +37,8 @@
 #include <cstdio>
 #include <mutex>
 #include <type_traits>
+#include <utility>
+#include <vector>
 
 #include "emb_internal.cuh"
 
@@ -120,13 +123,28 @@ __device__ __forceinline__ unsigned lanemask_lt() {
 
 // ------------------------------------------------------------------ 1. expand
 
-__global__ void ws_header_kernel(WsHeader* hdr, unsigned nnz, unsigned n_bags, unsigned sorted_in_b, unsigned miss) {
-  hdr->magic = kMagic;
-  hdr->nnz = nnz;
-  hdr->n_bags = n_bags;
-  hdr->sorted_in_b = sorted_in_b;
-  hdr->miss_row = miss;
-  hdr->n_unique = 0;
+// Header of a recording forward, launched before it with one block.  With
+// malformed (flagged) offsets some positions lie outside every bag: before
+// the first offset or at or after the last one (clamped to [0, nnz]; between
+// them every position is inside some bag).  They are written here as absent
+// pairs (row n_rows, bag n_bags), so no later kernel reads a stale pair; the
+// forward that follows overwrites every position that is inside a bag.
+__global__ void ws_header_kernel(WsHeader* hdr, unsigned nnz, unsigned n_bags, unsigned sorted_in_b, unsigned miss,
+                                 const long long* __restrict__ offsets, unsigned* __restrict__ K,
+                                 unsigned* __restrict__ V) {
+  if (threadIdx.x == 0) {
+    hdr->magic = kMagic;
+    hdr->nnz = nnz;
+    hdr->n_bags = n_bags;
+    hdr->sorted_in_b = sorted_in_b;
+    hdr->miss_row = miss;
+    hdr->n_unique = 0;
+  }
+  // no bags: every position is outside
+  const long long lo = n_bags == 0 ? (long long)nnz : min(max(offsets[0], 0LL), (long long)nnz);
+  const long long hi = n_bags == 0 ? (long long)nnz : min(max(offsets[n_bags], 0LL), (long long)nnz);
+  for (long long i = threadIdx.x; i < lo; i += blockDim.x) { K[i] = miss; V[i] = n_bags; }
+  for (long long i = hi + threadIdx.x; i < (long long)nnz; i += blockDim.x) { K[i] = miss; V[i] = n_bags; }
 }
 
 __global__ void __launch_bounds__(256) expand_kernel(TableView t, const long long* __restrict__ offsets,
@@ -146,6 +164,8 @@ __global__ void __launch_bounds__(256) expand_kernel(TableView t, const long lon
   }
   const long long nwarps = ((long long)gridDim.x * blockDim.x) >> 5;
   const unsigned S = (unsigned)t.n_slots;
+  if (n_bags == 0 && gw == 0)  // no bags: every position is absent
+    for (long long i = lane; i < nnz; i += 32) { K[i] = t.n_rows; V[i] = 0u; }
   for (long long bag = gw; bag < n_bags; bag += nwarps) {
     const int s = (int)((unsigned)bag % S);
     long long start = offsets[bag], end = offsets[bag + 1];
@@ -155,6 +175,13 @@ __global__ void __launch_bounds__(256) expand_kernel(TableView t, const long lon
       end = min(max(end, start), nnz);
     }
     if (mean && lane == 0) scale[bag] = end > start ? 1.0f / (float)(end - start) : 0.f;
+    // with malformed (flagged) offsets, positions before the first bag or after
+    // the last one belong to no bag: they become absent pairs, so no later
+    // kernel reads a stale pair
+    if (bag == 0)
+      for (long long i = lane; i < start; i += 32) { K[i] = t.n_rows; V[i] = (unsigned)n_bags; }
+    if (bag == n_bags - 1)
+      for (long long i = end + lane; i < nnz; i += 32) { K[i] = t.n_rows; V[i] = (unsigned)n_bags; }
     for (long long i = start + lane; i < end; i += 32) {
       const long long k = keys[i];
       unsigned row = t.n_rows, ext;
@@ -591,6 +618,40 @@ __device__ __forceinline__ void fma_x2(float* acc, float w, const float* g) {
   }
 }
 
+// Knuth's TwoSum on pairs of floats: s + x == t + e exactly with t = fl(s + x);
+// s becomes t and the rounding error e is added to the compensation c, so
+// s + c carries the running sum to about one rounding of its exact value
+// however long the run (a plain float32 running sum loses up to one ulp of
+// the running sum per addition).  Packed f32x2 arithmetic in inline PTX, so
+// no step is contracted or reassociated.
+template <int N>
+__device__ __forceinline__ void two_sum_x2(float* s, float* c, const float* x) {
+#pragma unroll
+  for (int i = 0; i < N; i += 2) {
+    unsigned long long S, X, C, T, Z, A, B;
+    asm("mov.b64 %0, {%1,%2};" : "=l"(S) : "f"(s[i]), "f"(s[i + 1]));
+    asm("mov.b64 %0, {%1,%2};" : "=l"(X) : "f"(x[i]), "f"(x[i + 1]));
+    asm("mov.b64 %0, {%1,%2};" : "=l"(C) : "f"(c[i]), "f"(c[i + 1]));
+    asm("add.rn.f32x2 %0, %1, %2;" : "=l"(T) : "l"(S), "l"(X));  // t = s + x
+    asm("sub.rn.f32x2 %0, %1, %2;" : "=l"(Z) : "l"(T), "l"(S));  // z = t - s
+    asm("sub.rn.f32x2 %0, %1, %2;" : "=l"(A) : "l"(T), "l"(Z));  // t - z
+    asm("sub.rn.f32x2 %0, %1, %2;" : "=l"(A) : "l"(S), "l"(A));  // s - (t - z)
+    asm("sub.rn.f32x2 %0, %1, %2;" : "=l"(B) : "l"(X), "l"(Z));  // x - z
+    asm("add.rn.f32x2 %0, %1, %2;" : "=l"(A) : "l"(A), "l"(B));  // e
+    asm("add.rn.f32x2 %0, %1, %2;" : "=l"(C) : "l"(C), "l"(A));  // c += e
+    asm("mov.b64 {%0,%1}, %2;" : "=f"(s[i]), "=f"(s[i + 1]) : "l"(T));
+    asm("mov.b64 {%0,%1}, %2;" : "=f"(c[i]), "=f"(c[i + 1]) : "l"(C));
+  }
+}
+
+// The same TwoSum step on one float.
+__device__ __forceinline__ void two_sum(float& s, float& c, float x) {
+  const float t = __fadd_rn(s, x);
+  const float z = __fsub_rn(t, s);
+  c = __fadd_rn(c, __fadd_rn(__fsub_rn(s, __fsub_rn(t, z)), __fsub_rn(x, z)));
+  s = t;
+}
+
 struct StageMeta {
   long long e0;
   unsigned row;
@@ -608,8 +669,11 @@ struct StageMeta {
 // into L2.  The group then walks the window in order, U positions at a time:
 // per position one broadcast read of the record and one vector load per
 // column block, then multiply-adds; a group of U positions with no row start
-// in it adds without any per-position test.  At a row start the finished row
-// is staged in shared memory.  Staged rows are then applied (Adagrad on a
+// in it adds without any per-position test.  The U products of a group are
+// summed plainly and the group's sum is folded into the row's running sum
+// with TwoSum (a compensated float32 sum: about one rounding of the exact
+// per-key gradient however many occurrences a hot key has).  At a row start
+// the finished row is staged in shared memory.  Staged rows are then applied (Adagrad on a
 // whole segment) or parked (partial of a segment cut by a sub-chunk edge) by
 // one copy of that code, outside the unrolled walk.
 constexpr int kRedWarps = 4;  // warps per reduce block
@@ -670,11 +734,12 @@ __global__ void __launch_bounds__(kRedWarps * 32, 10) segreduce_adagrad_kernel(
     unsigned cur = kNoRow;
     bool cur_starts = first_starts;
     RowGeo cg{0, 0, 0, false};
-    float acc[NCB][VW];
+    float acc[NCB][VW];  // running sum of the row
+    float cmp[NCB][VW];  // its TwoSum compensation
 #pragma unroll
     for (int cc = 0; cc < NCB; ++cc)
 #pragma unroll
-      for (int j = 0; j < VW; ++j) acc[cc][j] = 0.f;
+      for (int j = 0; j < VW; ++j) acc[cc][j] = cmp[cc][j] = 0.f;
 
     // stage the finished row `cur` (no-op for misses and stale rows)
     auto stage_cur = [&](int slot, bool ends) {
@@ -683,7 +748,8 @@ __global__ void __launch_bounds__(kRedWarps * 32, 10) segreduce_adagrad_kernel(
 #pragma unroll
         for (int j = 0; j < VW; j += 4)
           *reinterpret_cast<float4*>(&st[slot][(cc * G + li) * VW + j]) =
-              make_float4(acc[cc][j], acc[cc][j + 1], acc[cc][j + 2], acc[cc][j + 3]);
+              make_float4(__fadd_rn(acc[cc][j], cmp[cc][j]), __fadd_rn(acc[cc][j + 1], cmp[cc][j + 1]),
+                          __fadd_rn(acc[cc][j + 2], cmp[cc][j + 2]), __fadd_rn(acc[cc][j + 3], cmp[cc][j + 3]));
       if (li == 0) mt[slot] = StageMeta{cg.e0, cur, (cur < miss && cg.ok) ? cg.D : 0,
                                         (cur_starts ? 1 : 0) | (ends ? 2 : 0)};
     };
@@ -775,11 +841,19 @@ __global__ void __launch_bounds__(kRedWarps * 32, 10) segreduce_adagrad_kernel(
         }
         const unsigned grp = (smask >> j0) & ((1u << UW) - 1u);
         if (grp == 0) {
+          float blk[NCB][VW];  // plain sum of the group's products
+#pragma unroll
+          for (int cc = 0; cc < NCB; ++cc)
+#pragma unroll
+            for (int q = 0; q < VW; ++q) blk[cc][q] = 0.f;
 #pragma unroll
           for (int u = 0; u < UW; ++u)
 #pragma unroll
-            for (int cc = 0; cc < NCB; ++cc) fma_vw<VW>(acc[cc], wv[u], gv[u][cc].v);
+            for (int cc = 0; cc < NCB; ++cc) fma_vw<VW>(blk[cc], wv[u], gv[u][cc].v);
+#pragma unroll
+          for (int cc = 0; cc < NCB; ++cc) two_sum_x2<VW>(acc[cc], cmp[cc], blk[cc]);
         } else {
+          // a row starts in this group: every product is folded in on its own
           int ns = 0;
 #pragma unroll
           for (int u = 0; u < UW; ++u) {
@@ -793,10 +867,16 @@ __global__ void __launch_bounds__(kRedWarps * 32, 10) segreduce_adagrad_kernel(
 #pragma unroll
               for (int cc = 0; cc < NCB; ++cc)
 #pragma unroll
-                for (int q = 0; q < VW; ++q) acc[cc][q] = 0.f;
+                for (int q = 0; q < VW; ++q) acc[cc][q] = cmp[cc][q] = 0.f;
             }
 #pragma unroll
-            for (int cc = 0; cc < NCB; ++cc) fma_vw<VW>(acc[cc], wv[u], gv[u][cc].v);
+            for (int cc = 0; cc < NCB; ++cc) {
+              float p[VW];
+#pragma unroll
+              for (int q = 0; q < VW; ++q) p[q] = 0.f;
+              fma_vw<VW>(p, wv[u], gv[u][cc].v);
+              two_sum_x2<VW>(acc[cc], cmp[cc], p);
+            }
           }
           if (ns) drain(ns);
         }
@@ -846,11 +926,11 @@ __global__ void __launch_bounds__(256) fixup_kernel(TableView t, const unsigned*
     const unsigned m = c1 - c + 1;
     const unsigned per = (m + P - 1) / P;
     const unsigned j0 = sub * per, j1 = min(m, j0 + per);
-    float acc[NCB][4];
+    float acc[NCB][4], cmp[NCB][4];  // compensated (TwoSum) sums of the partial rows
 #pragma unroll
     for (int cc = 0; cc < NCB; ++cc)
 #pragma unroll
-      for (int j = 0; j < 4; ++j) acc[cc][j] = 0.f;
+      for (int j = 0; j < 4; ++j) acc[cc][j] = cmp[cc][j] = 0.f;
     for (unsigned jb = j0; jb < j1; jb += 4) {
       float4 x[4][NCB];
 #pragma unroll
@@ -869,20 +949,28 @@ __global__ void __launch_bounds__(256) fixup_kernel(TableView t, const unsigned*
         if (jb + q < j1) {
 #pragma unroll
           for (int cc = 0; cc < NCB; ++cc) {
-            acc[cc][0] += x[q][cc].x;
-            acc[cc][1] += x[q][cc].y;
-            acc[cc][2] += x[q][cc].z;
-            acc[cc][3] += x[q][cc].w;
+            two_sum(acc[cc][0], cmp[cc][0], x[q][cc].x);
+            two_sum(acc[cc][1], cmp[cc][1], x[q][cc].y);
+            two_sum(acc[cc][2], cmp[cc][2], x[q][cc].z);
+            two_sum(acc[cc][3], cmp[cc][3], x[q][cc].w);
           }
         }
       }
     }
-    // groups hold consecutive ranges: combine with a fixed xor tree
+    // groups hold consecutive ranges: combine (sum, compensation) pairs with a
+    // fixed xor tree, then round each to one float
 #pragma unroll
     for (int cc = 0; cc < NCB; ++cc)
 #pragma unroll
-      for (int j = 0; j < 4; ++j)
-        for (int off = G; off < 32; off <<= 1) acc[cc][j] += __shfl_xor_sync(0xffffffffu, acc[cc][j], off);
+      for (int j = 0; j < 4; ++j) {
+        for (int off = G; off < 32; off <<= 1) {
+          const float so = __shfl_xor_sync(0xffffffffu, acc[cc][j], off);
+          const float co = __shfl_xor_sync(0xffffffffu, cmp[cc][j], off);
+          two_sum(acc[cc][j], cmp[cc][j], so);
+          cmp[cc][j] = __fadd_rn(cmp[cc][j], co);
+        }
+        acc[cc][j] = __fadd_rn(acc[cc][j], cmp[cc][j]);
+      }
     if (sub == 0) adagrad_row<TW, NCB>(t, e0, D, G, li, acc, lr, eps);
   }
 }
@@ -1079,9 +1167,9 @@ static emb_status run_bwd(emb_table* table, const int64_t* offsets_d, int64_t n_
   float* scale = (float*)(ws + L.scale);
   const int mean = pool == EMB_POOL_MEAN;
 
-  // With malformed offsets (flagged) some positions keep stale values; every
-  // later kernel treats rows >= n_rows and bags >= n_bags as absent, so they
-  // stay in bounds.
+  // With malformed offsets (flagged) the expand step (or the recording
+  // forward) writes positions outside every bag as absent pairs; every later
+  // kernel treats rows >= n_rows and bags >= n_bags as absent.
   if (!recorded) {
     long long blocks = std::min<long long>((n_bags * 32 + 255) / 256, resident_blocks(256));
     expand_kernel<<<(int)std::max(1LL, blocks), 256, 0, st>>>(v, (const long long*)offsets_d, n_bags,
@@ -1128,25 +1216,61 @@ static emb_status run_bwd(emb_table* table, const int64_t* offsets_d, int64_t n_
 // Scratch for emb_bwd_adagrad_noalloc, for callers that cannot allocate
 // device memory.  The loader reserves it on every GPU that loads this library;
 // host code must not pass the symbol itself to a kernel (on the host it only
-// names a stand-in), so each device's address is looked up once.
+// names a stand-in), so its device address is looked up with
+// cudaGetSymbolAddress, once per CUDA context: a context that is destroyed
+// (cudaDeviceReset) and created again reloads the module, and the array may
+// then sit at another address, so the cache is keyed by the context's
+// unique id, not by the device index.
 static __device__ __align__(256) unsigned char g_noalloc_scratch[EMB_NOALLOC_SCRATCH_BYTES];
 
-constexpr int kMaxDevices = 64;
+typedef int (*CtxGetCurrentFn)(void** ctx);
+typedef int (*CtxGetIdFn)(void* ctx, unsigned long long* id);
+
 static std::mutex g_noalloc_mu;
-static void* g_noalloc_ptr[kMaxDevices] = {};
+static std::vector<std::pair<unsigned long long, void*>> g_noalloc_ptr;  // (context id, scratch address)
+
+// Unique id of the calling thread's current context (0 if none is current),
+// through the driver entry points the runtime hands out (the library links
+// no driver library directly).
+static emb_status current_context_id(unsigned long long* id) {
+  static CtxGetCurrentFn get_cur = nullptr;
+  static CtxGetIdFn get_id = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", (void**)&get_cur, 12000, cudaEnableDefault, &q) !=
+            cudaSuccess || q != cudaDriverEntryPointSuccess)
+      get_cur = nullptr;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetId", (void**)&get_id, 12000, cudaEnableDefault, &q) !=
+            cudaSuccess || q != cudaDriverEntryPointSuccess)
+      get_id = nullptr;
+    cudaGetLastError();
+  });
+  if (!get_cur || !get_id) return fail(EMB_ERR_CUDA, "driver entry points cuCtxGetCurrent/cuCtxGetId unavailable");
+  void* ctx = nullptr;
+  if (get_cur(&ctx) != 0) return fail(EMB_ERR_CUDA, "cuCtxGetCurrent failed");
+  *id = 0;
+  if (ctx && get_id(ctx, id) != 0) return fail(EMB_ERR_CUDA, "cuCtxGetId failed");
+  return EMB_OK;
+}
 
 static emb_status noalloc_scratch(void** out) {
-  int dev = 0;
-  EMB_CUDA(cudaGetDevice(&dev));
-  if (dev < 0 || dev >= kMaxDevices) return fail(EMB_ERR_UNSUPPORTED, "device index beyond the no-alloc table");
+  unsigned long long id = 0;
+  emb_status rc = current_context_id(&id);
+  if (rc != EMB_OK) return rc;
   std::lock_guard<std::mutex> g(g_noalloc_mu);
-  if (!g_noalloc_ptr[dev]) {
-    void* p = nullptr;
-    cudaError_t e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
-    if (e != cudaSuccess) return cuda_fail(e, "cudaGetSymbolAddress(no-alloc scratch)");
-    g_noalloc_ptr[dev] = p;
-  }
-  *out = g_noalloc_ptr[dev];
+  if (id != 0)
+    for (const auto& e : g_noalloc_ptr)
+      if (e.first == id) {
+        *out = e.second;
+        return EMB_OK;
+      }
+  void* p = nullptr;
+  cudaError_t e = cudaGetSymbolAddress(&p, g_noalloc_scratch);  // also makes the device's context current
+  if (e != cudaSuccess) return cuda_fail(e, "cudaGetSymbolAddress(no-alloc scratch)");
+  if (id == 0 && (rc = current_context_id(&id)) != EMB_OK) return rc;
+  if (id != 0) g_noalloc_ptr.emplace_back(id, p);
+  *out = p;
   return EMB_OK;
 }
 
@@ -1189,8 +1313,9 @@ emb_status emb_lookup_fwd_record(emb_table* table, const int64_t* offsets_d, int
   if (((uintptr_t)workspace_d & 255) != 0) return fail(EMB_ERR_WORKSPACE, "workspace must be 256-byte aligned");
   cudaStream_t st = (cudaStream_t)stream;
   char* ws = (char*)workspace_d;
-  ws_header_kernel<<<1, 1, 0, st>>>((WsHeader*)(ws + L.hdr), (unsigned)nnz, (unsigned)n_bags,
-                                    (unsigned)(sort_passes(table) & 1), (unsigned)table->st.n_keys);
+  ws_header_kernel<<<1, 256, 0, st>>>((WsHeader*)(ws + L.hdr), (unsigned)nnz, (unsigned)n_bags,
+                                      (unsigned)(sort_passes(table) & 1), (unsigned)table->st.n_keys,
+                                      (const long long*)offsets_d, (unsigned*)(ws + L.kA), (unsigned*)(ws + L.vA));
   if (n_bags > 0) {
     // bags are handed out in order from a counter (measured 17.7 -> 15.1 ms at
     // 100M keys x dim 128 against a static order; Zipf bag lengths unbalance it)

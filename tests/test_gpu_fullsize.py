@@ -1,5 +1,8 @@
 """GPU parity at the five workloads' full sizes, in the benchmark's launch
-configuration, on outputs the oracle computes one by one:
+configuration (the recording forward emb_lookup_fwd_record + the recorded
+backward emb_bwd_adagrad_recorded, as the benchmark times them; the
+unrecorded pair emb_lookup_fwd + emb_bwd_adagrad on the 26-slot workload),
+on outputs the oracle computes one by one:
 
 * slot resolution and hit/miss: bit-exact on a random sample of occurrences;
 * pooled output: sampled bags (random and the longest ones);
@@ -20,7 +23,7 @@ import torch
 import oracle
 import workload as W
 import sparse_ctr_embedding_gb300 as E
-from parity_util import acc_scale, gate, plain_rel, tol_of, w_scale
+from parity_util import acc_scale, gate, plain_rel, report, tol_of, w_scale
 
 pytestmark = [pytest.mark.gpu, pytest.mark.slow]
 
@@ -32,7 +35,7 @@ def built():
 
 
 class FullRun:
-    def __init__(self, i):
+    def __init__(self, i, recorded=True):
         cfg = W.config(i)
         self.cfg = cfg
         dev = torch.device("cuda")
@@ -54,8 +57,13 @@ class FullRun:
         self.w_before, self.a_before = E.emb_table_export_rows(tbl, self.rand_rows)
         out = torch.empty((cfg.batch, cfg.sum_dims), dtype=torch.float32, device=dev)
         ws = torch.empty(E.emb_bwd_workspace_size(tbl, n_bags, nnz), dtype=torch.uint8, device=dev)
-        E.emb_lookup_fwd(tbl, off, q, cfg.pool, out=out)
-        E.emb_bwd_adagrad(tbl, off, q, cfg.pool, grad, cfg.lr, cfg.eps, ws)
+        if recorded:   # the benchmark's step
+            E.emb_lookup_fwd_record(tbl, off, q, cfg.pool, ws, out=out)
+            E.emb_bwd_adagrad_recorded(tbl, n_bags, nnz, cfg.pool, grad, cfg.lr, cfg.eps, ws)
+        else:
+            E.emb_lookup_fwd(tbl, off, q, cfg.pool, out=out)
+            E.emb_bwd_adagrad(tbl, off, q, cfg.pool, grad, cfg.lr, cfg.eps, ws)
+        self.path = "recorded" if recorded else "unrecorded"
         uk = torch.empty(nnz, dtype=torch.int64, device=dev)
         nu = torch.zeros(1, dtype=torch.int64, device=dev)
         E.emb_bwd_unique_keys(tbl, ws, uk, nu)
@@ -85,9 +93,10 @@ class FullRun:
         self.tbl.close()
 
 
-@pytest.fixture(scope="module", params=[1, 2, 3, 4, 5], ids=lambda i: f"config{i}")
+@pytest.fixture(scope="module", params=[(1, True), (2, True), (2, False), (3, True), (4, True), (5, True)],
+                ids=lambda p: f"config{p[0]}-{'recorded' if p[1] else 'unrecorded'}")
 def run(request):
-    r = FullRun(request.param)
+    r = FullRun(*request.param)
     yield r
     r.close()
     del r
@@ -146,7 +155,7 @@ def test_pooled_output_on_sampled_bags(run):
     cols = np.concatenate([[0], np.cumsum(cfg.dims)])
     got = np.concatenate([out[b // cfg.n_slots, cols[b % cfg.n_slots]:cols[b % cfg.n_slots + 1]] for b in bags])
     rel = gate("pooled", got, ref, np.maximum(np.abs(ref), A), tol_of(cfg))
-    print(cfg.name, "pooled gate", rel, "plain", plain_rel(got, ref))
+    report(f"full/{cfg.name}/{run.path}", pooled_gate=rel, pooled_plain_rel=plain_rel(got, ref), bags=int(bags.size))
 
 
 def test_adagrad_on_hot_and_sampled_keys(run):
@@ -168,10 +177,11 @@ def test_adagrad_on_hot_and_sampled_keys(run):
     w_x = wg.cpu().numpy().reshape(-1)[mask].astype(np.float64)
     a_x = ag.cpu().numpy().reshape(-1)[mask]
     tol = tol_of(cfg)
-    ga = gate("acc", a_x, acc_r, acc_scale(acc_r, G, Ag, tol), tol)
-    gw = gate("weight", w_x, w_r.astype(np.float64), w_scale(w_r, vals[idx], acc_r, Ag, cfg.lr), tol)
-    print(cfg.name, f"{pick.size} keys ({hot.size} hottest)", "acc gate", ga, "w gate", gw,
-          "plain acc", plain_rel(a_x, acc_r), "plain w", plain_rel(w_x, w_r))
+    ga = gate("acc", a_x, acc_r, acc_scale(acc_r), tol)
+    gw = gate("weight", w_x, w_r.astype(np.float64), w_scale(w_r, vals[idx]), tol)
+    cond = float((Ag / np.maximum(np.abs(G), 1e-300)).max())   # A_g / |g|: how much the key's terms cancel
+    report(f"full/{cfg.name}/{run.path}", keys=int(pick.size), hottest=int(hot.size), acc_gate=ga, w_gate=gw,
+           acc_plain_rel=plain_rel(a_x, acc_r), w_plain_rel=plain_rel(w_x, w_r), max_cancellation=cond)
 
 
 def test_untouched_rows_bit_identical(run):

@@ -8,7 +8,7 @@ import torch
 import oracle
 import workload as W
 import sparse_ctr_embedding_gb300 as E
-from parity_util import check_step, gpu_step, make_table, tol_of
+from parity_util import check_step, gpu_step, make_table, report, tol_of
 
 pytestmark = pytest.mark.gpu
 
@@ -33,7 +33,7 @@ def test_step_parity_small(cfg):
     wl = W.make(cfg, device="cuda")
     gs = gpu_step(cfg, wl)
     rep = check_step(cfg, wl, gs)
-    print(cfg.name, rep)
+    report(f"small/{cfg.name}/unrecorded", **rep)
 
 
 @pytest.mark.parametrize("cfg", SMALL, ids=lambda c: c.name)
@@ -42,7 +42,7 @@ def test_recorded_step_parity_and_identity(cfg):
     from them: oracle parity, and bit-identical to the unrecorded path."""
     wl = W.make(cfg, device="cuda")
     rec = gpu_step(cfg, wl, recorded=True)
-    check_step(cfg, wl, rec)
+    report(f"small/{cfg.name}/recorded", **check_step(cfg, wl, rec))
     ref = gpu_step(cfg, wl)
     assert torch.equal(rec.out, ref.out)
     assert np.array_equal(rec.values_out.view(np.uint8), ref.values_out.view(np.uint8))

@@ -209,16 +209,20 @@ def _random_case(seed, n_keys=300, n_slots=3, D=8, B=40, max_len=12, absent_p=0.
     return keys, values, off, q, grad
 
 
+@pytest.mark.parametrize("wd", [np.float32, np.float16], ids=["f32", "f16"])
 @pytest.mark.parametrize("pool", ["sum", "mean"])
-def test_forward_matches_torch_embedding_bag(pool):
-    keys, values, off, q, _ = _random_case(11, absent_p=0.0)
+def test_forward_matches_torch_embedding_bag(pool, wd):
+    """Float32 and float16 rows: the half rows are read by the oracle's own
+    half loader and by numpy's exact half -> double conversion here, so a
+    wrong element width, offset or conversion in the former fails."""
+    keys, values, off, q, _ = _random_case(11, absent_p=0.0, wd=wd)
     n_slots, D = 3, 8
     T = oracle.Table(keys, 1024, [D] * n_slots)
-    out, A = T.forward(off, q, pool, "f32", values.reshape(-1))
+    out, A = T.forward(off, q, pool, "f16" if wd == np.float16 else "f32", values.reshape(-1))
     # library routine: EmbeddingBag over dense row indices (independent dict lookup)
     idx = {int(k): i for i, k in enumerate(keys)}
     flat = torch.tensor([idx[int(k)] for k in q], dtype=torch.int64)
-    ref = torch.nn.functional.embedding_bag(flat, torch.from_numpy(values).double(),
+    ref = torch.nn.functional.embedding_bag(flat, torch.from_numpy(values.astype(np.float64)),
                                             torch.from_numpy(off[:-1]), mode=pool)
     np.testing.assert_allclose(out.reshape(-1, D), ref.numpy(), rtol=1e-13, atol=1e-13)
     assert np.all(A.reshape(-1, D) >= np.abs(out.reshape(-1, D)) - 1e-12)
@@ -243,13 +247,15 @@ def test_backward_matches_torch_autograd(pool):
         np.testing.assert_allclose(G[goff[i]:goff[i + 1]], ref[r], rtol=1e-12, atol=1e-12)
 
 
-def test_pooling_brute_force_with_misses_and_special_cases():
-    keys, values, off, q, grad = _random_case(13, absent_p=0.3, max_len=6)
+@pytest.mark.parametrize("wd", [np.float32, np.float16], ids=["f32", "f16"])
+def test_pooling_brute_force_with_misses_and_special_cases(wd):
+    keys, values, off, q, grad = _random_case(13, absent_p=0.3, max_len=6, wd=wd)
     n_slots, D = 3, 8
     T = oracle.Table(keys, 1024, [D] * n_slots)
     table = {int(k): values[i].astype(np.float64) for i, k in enumerate(keys)}
-    s_out, _ = T.forward(off, q, "sum", "f32", values.reshape(-1))
-    m_out, _ = T.forward(off, q, "mean", "f32", values.reshape(-1))
+    wname = "f16" if wd == np.float16 else "f32"
+    s_out, _ = T.forward(off, q, "sum", wname, values.reshape(-1))
+    m_out, _ = T.forward(off, q, "mean", wname, values.reshape(-1))
     s_out = s_out.reshape(-1, D); m_out = m_out.reshape(-1, D)
     for bag in range(off.size - 1):
         ks = q[off[bag]:off[bag + 1]]

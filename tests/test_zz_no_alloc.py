@@ -1,16 +1,18 @@
 """emb_bwd_adagrad_noalloc: the backward + Adagrad step for callers that cannot
 allocate device memory (a framework's caching allocator already owns the GPU,
-or a serving loop that forbids allocation during a step).  It must give the
-same table update as emb_bwd_adagrad with a caller workspace, call after call,
-through the C ABI.  This file sorts last so a stop-at-first-failure run has
-already run every other test."""
+or a serving loop that forbids allocation during a step).  It runs the same
+kernels as emb_bwd_adagrad with a caller workspace, so it must give a
+bitwise-identical table update, call after call, through the C ABI, whatever
+an earlier call left in the library's shared scratch array.  This file sorts
+last so a stop-at-first-failure run has already run every other test."""
 import numpy as np
 import pytest
 import torch
 
+import oracle
 import workload as W
 import sparse_ctr_embedding_gb300 as E
-from parity_util import gate, make_table, tol_of
+from parity_util import acc_scale, elem_index, gate, make_table, tol_of, w_scale
 
 pytestmark = pytest.mark.gpu
 
@@ -21,33 +23,97 @@ def built():
     assert torch.cuda.is_available(), "GPU tests need a CUDA device"
 
 
-def _export(cfg, tbl, n_el, dt):
+def _export(tbl, n_el, dt):
     vo = torch.empty(n_el, dtype=dt, device="cuda")
     ao = torch.empty(n_el, dtype=torch.float32, device="cuda")
     E.emb_table_export(tbl, None, vo, ao)
-    return vo.double().cpu().numpy(), ao.double().cpu().numpy()
+    return vo.cpu().numpy(), ao.cpu().numpy()
 
 
-@pytest.mark.parametrize("cfg", [W.config(1), W.scaled(W.config(5), 1000, 256)], ids=lambda c: c.name)
+def _bits(a):
+    return np.ascontiguousarray(a).view(np.uint8)
+
+
+LARGE = W.scaled(W.config(5), 1000, 256)   # 64 slots, dim 128 f16, long bags, hot keys
+SMALL = W.config(1)                        # 4 slots, dim 16 f32
+
+
+@pytest.mark.parametrize("cfg", [SMALL, LARGE], ids=lambda c: c.name)
 def test_noalloc_matches_workspace_path_on_two_calls(cfg):
     wl = W.make(cfg, device="cuda")
     off, q, g = wl.offsets, wl.qkeys, wl.grad
     n_bags, nnz = off.numel() - 1, q.numel()
-    assert E.emb_bwd_workspace_size(make_table(cfg, wl), n_bags, nnz) <= E.EMB_NOALLOC_SCRATCH_BYTES
     ref = make_table(cfg, wl)
     new = make_table(cfg, wl)
+    assert E.emb_bwd_workspace_size(ref, n_bags, nnz) <= E.EMB_NOALLOC_SCRATCH_BYTES
     ws = torch.empty(E.emb_bwd_workspace_size(ref, n_bags, nnz), dtype=torch.uint8, device="cuda")
     n_el = ref.stats["n_elems"]
-    tol = tol_of(cfg)
     for call in range(2):
         E.emb_bwd_adagrad(ref, off, q, cfg.pool, g, cfg.lr, cfg.eps, ws)
         E.emb_bwd_adagrad_noalloc(new, off, q, cfg.pool, g, cfg.lr, cfg.eps)
         assert E.emb_check_device_flag(new) == 0
-        w_r, a_r = _export(cfg, ref, n_el, wl.values.dtype)
-        w_x, a_x = _export(cfg, new, n_el, wl.values.dtype)
-        gate(f"weights after call {call + 1}", w_x, w_r, np.maximum(np.abs(w_r), 1e-30), tol)
-        gate(f"accumulators after call {call + 1}", a_x, a_r, a_r, tol)
+        w_r, a_r = _export(ref, n_el, wl.values.dtype)
+        w_x, a_x = _export(new, n_el, wl.values.dtype)
+        assert np.array_equal(_bits(w_x), _bits(w_r)), f"weights differ after call {call + 1}"
+        assert np.array_equal(_bits(a_x), _bits(a_r)), f"accumulators differ after call {call + 1}"
         assert not np.array_equal(a_r, np.full_like(a_r, cfg.acc0))   # the step did update rows
+
+
+def _oracle_step(cfg, wl):
+    """The oracle's table after one step from the initial state: (weights, accumulators)."""
+    keys, off, q = wl.keys.cpu().numpy(), wl.offsets.cpu().numpy(), wl.qkeys.cpu().numpy()
+    values, grad = wl.values.cpu().numpy(), wl.grad.cpu().numpy()
+    T = oracle.Table(keys, cfg.capacity, cfg.dims)
+    _, rows_u, _, G, _ = T.backward(off, q, cfg.pool, grad)
+    idx = elem_index(T.elem_offsets(), rows_u)
+    w_r, acc_r = oracle.adagrad(G, values[idx], np.full(idx.size, cfg.acc0, np.float32), cfg.lr, cfg.eps)
+    return idx, w_r, acc_r
+
+
+def test_large_call_then_smaller_call_in_the_shared_scratch():
+    """A large batch fills much of the shared array; a smaller one after it must
+    not read anything the large one left there (every region it reads is
+    written first).  Each is checked bitwise against the workspace path on its
+    own table and against the oracle."""
+    for cfg in (LARGE, SMALL):
+        wl = W.make(cfg, device="cuda")
+        off, q, g = wl.offsets, wl.qkeys, wl.grad
+        n_bags, nnz = off.numel() - 1, q.numel()
+        ref, new = make_table(cfg, wl), make_table(cfg, wl)
+        ws = torch.empty(E.emb_bwd_workspace_size(ref, n_bags, nnz), dtype=torch.uint8, device="cuda")
+        E.emb_bwd_adagrad(ref, off, q, cfg.pool, g, cfg.lr, cfg.eps, ws)
+        E.emb_bwd_adagrad_noalloc(new, off, q, cfg.pool, g, cfg.lr, cfg.eps)
+        assert E.emb_check_device_flag(new) == 0
+        n_el = ref.stats["n_elems"]
+        w_r, a_r = _export(ref, n_el, wl.values.dtype)
+        w_x, a_x = _export(new, n_el, wl.values.dtype)
+        assert np.array_equal(_bits(w_x), _bits(w_r)) and np.array_equal(_bits(a_x), _bits(a_r)), cfg.name
+        idx, w_o, a_o = _oracle_step(cfg, wl)
+        tol = tol_of(cfg)
+        gate(f"{cfg.name} accumulators", a_x[idx], a_o, acc_scale(a_o), tol)
+        gate(f"{cfg.name} weights", w_x[idx].astype(np.float64), w_o.astype(np.float64),
+             w_scale(w_o, wl.values.cpu().numpy()[idx]), tol)
+        ref.close()
+        new.close()
+
+
+def test_malformed_offsets_after_a_full_call_update_nothing():
+    """After a normal call has left its (row, bag) pairs in the shared array, a
+    call whose offsets end before nnz (every bag empty) must update no row:
+    positions outside every bag are absent pairs, never the earlier call's."""
+    cfg = LARGE
+    wl = W.make(cfg, device="cuda")
+    off, q, g = wl.offsets, wl.qkeys, wl.grad
+    tbl = make_table(cfg, wl)
+    E.emb_bwd_adagrad_noalloc(tbl, off, q, cfg.pool, g, cfg.lr, cfg.eps)
+    assert E.emb_check_device_flag(tbl) == 0
+    n_el = tbl.stats["n_elems"]
+    w0, a0 = _export(tbl, n_el, wl.values.dtype)
+    empty = torch.zeros_like(off)                     # offsets[n_bags] = 0 < nnz: flagged, all bags empty
+    E.emb_bwd_adagrad_noalloc(tbl, empty, q, cfg.pool, g, cfg.lr, cfg.eps)
+    assert E.emb_check_device_flag(tbl) & E.EMB_FLAG_BAD_OFFSETS
+    w1, a1 = _export(tbl, n_el, wl.values.dtype)
+    assert np.array_equal(_bits(w1), _bits(w0)) and np.array_equal(_bits(a1), _bits(a0))
 
 
 def test_noalloc_rejects_batches_beyond_its_scratch():
