@@ -165,11 +165,14 @@ def max_over_ranks(ws, x: float) -> float:
     return float(t.item())
 
 
-def launches_per_step(n_keys: int, digit_bits: int) -> int:
-    """Kernels this library launches for one recording fwd + one recorded bwd call."""
-    bits = max(1, int(n_keys).bit_length())
+def launches_per_step(max_slot_keys: int, digit_bits: int) -> int:
+    """Kernels this library launches for one recording fwd + one recorded bwd call.
+    The backward sorts rows within a slot, so the pass count follows the largest slot."""
+    bits = max(1, int(max_slot_keys).bit_length())
     passes = max(1, math.ceil(bits / digit_bits))
-    return 2 + passes * 5 + 2   # header + recording fwd; (count + 3 scan + scatter) per radix pass; reduce; fixup
+    # placement (3 scan kernels + region setup) + recording fwd; (count + 3 scan + scatter)
+    # per radix pass; reduce; fixup
+    return 5 + passes * 5 + 2
 
 
 # ------------------------------------------------------------------ oracle (CPU baseline / reference arm)
@@ -347,13 +350,14 @@ def run_ours(args):
     # table updates the f32 master and writes the element's f16 copy
     rmw_bytes = int(d_u.sum()) * (2 * 4 + 8 + 2 if cfg.wdtype == "f16m" else 2 * wsz + 8)
     del uk, d_u
-    # the recording forward resolved every key once; the backward reads grad_out
-    # and read-modify-writes the hit rows (the cached row ids are workspace)
-    bwd_bytes = 4 * cfg.batch * cfg.sum_dims + rmw_bytes
+    # the backward's bytes: the cached 4-byte row id of every occurrence (what
+    # replaces the re-read of its key and the re-probe), the offsets, grad_out,
+    # and the read-modify-write of the hit rows
+    bwd_bytes = 4 * nnz + 8 * (n_bags + 1) + 4 * cfg.batch * cfg.sum_dims + rmw_bytes
     # algorithmic bytes per launch of each kernel (sort and partial sums are overhead)
     kernel_bytes = {
         "fwd_pool_kernel": fwd_bytes,
-        "segreduce_adagrad_kernel": 4 * cfg.batch * cfg.sum_dims + rmw_bytes,
+        "segreduce_update_kernel": 4 * cfg.batch * cfg.sum_dims + rmw_bytes,
     }
     flags = E.emb_check_device_flag(tbl)
 
@@ -391,9 +395,7 @@ def run_ours(args):
     flags |= E.emb_check_device_flag(tbl)
     kernel_ms = {"fwd_pool_kernel": fwd_ms,
                  "radix sort (count + scan + scatter kernels)": phase_ms["sort"],
-                 "segreduce_adagrad_kernel": phase_ms["reduce"], "fixup_kernel": phase_ms["fixup"]}
-    if cfg.wdtype == "f16m":
-        kernel_ms["refresh_half_kernel"] = statistics.mean(e[-2].elapsed_time(e[-1]) for e in ev)
+                 "segreduce_update_kernel": phase_ms["reduce"], "fixup_kernel": phase_ms["fixup"]}
 
     # ---- end to end through the C ABI: every step's CSR batch and grad_out are
     # copied in from pinned host memory and its pooled output copied back.  The
@@ -502,8 +504,7 @@ def run_ours(args):
         "fwd_roofline": {"achieved": fwd_gbs, "frac": fwd_gbs / peak, "algorithmic_bytes": fwd_bytes},
         "bwd_roofline": {"achieved": bwd_gbs, "frac": bwd_gbs / peak, "algorithmic_bytes": bwd_bytes},
         "cpu_baseline": cpu, "e2e": e2e,
-        "gpu_launches": K * (launches_per_step(st["n_keys"], E.EMB_SORT_DIGIT_BITS)
-                             + (1 if cfg.wdtype == "f16m" else 0)),   # + the f16 copy refresh
+        "gpu_launches": K * launches_per_step(st["max_slot_keys"], E.EMB_SORT_DIGIT_BITS),
         "clocks": clk, "device_flags": flags,
         "setup_s": {"generate": t_gen, "table_create": t_create},
     }

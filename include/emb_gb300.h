@@ -85,6 +85,12 @@ typedef enum {
  *     its master rounded to nearest-even.  10 bytes per element with the
  *     accumulator. */
 typedef enum { EMB_F32 = 0, EMB_F16 = 1, EMB_F16_MASTER = 2 } emb_dtype;
+
+/* The sparse optimizer a table is created for (JD ads article 3.2.1 names
+ * Adagrad and FTRL).  Adagrad keeps one f32 accumulator per element; FTRL
+ * keeps two f32 state values per element, n (in the accumulator array) and
+ * z.  A backward call of the other optimizer is refused. */
+typedef enum { EMB_OPT_ADAGRAD = 0, EMB_OPT_FTRL = 1 } emb_optimizer;
 typedef enum { EMB_POOL_SUM = 0, EMB_POOL_MEAN = 1 } emb_pool;
 
 /* Device flag bits reported by emb_check_device_flag. */
@@ -99,10 +105,12 @@ typedef enum { EMB_POOL_SUM = 0, EMB_POOL_MEAN = 1 } emb_pool;
 #define EMB_MAX_NNZ 2147483647LL   /* per call */
 #define EMB_MAX_BAGS 2147483647LL  /* per call */
 
-/* Digit width of the backward's stable radix sort of (row, bag) pairs: a
- * table of n keys sorts in ceil(bits(n) / EMB_SORT_DIGIT_BITS) passes, each
- * one digit-count, three scan and one scatter launch (no counterpart in the
- * pages; stated so callers can count the kernels a step launches). */
+/* Digit width of the backward's stable radix sort of (row, bag) pairs.  The
+ * pairs are placed slot by slot, so only the row number within a slot is
+ * sorted: ceil(bits(max_slot_keys) / EMB_SORT_DIGIT_BITS) passes (at least
+ * one), each one digit-count, three scan and one scatter launch (no
+ * counterpart in the pages; stated so callers can count the kernels a step
+ * launches). */
 #define EMB_SORT_DIGIT_BITS 7
 
 typedef struct {
@@ -110,8 +118,18 @@ typedef struct {
   const int32_t* slot_dim; /* host [n_slots]: embedding dim of each slot */
   emb_dtype wdtype;        /* weight storage type */
   int64_t capacity;        /* slots: power of two >= 2*n_keys; 0 = the smallest such */
-  float acc_init;          /* accumulator value used when emb_table_create gets acc == NULL */
+  float acc_init;          /* accumulator (FTRL: n) value used when emb_table_create gets acc == NULL */
+  emb_optimizer optimizer; /* EMB_OPT_ADAGRAD (0) or EMB_OPT_FTRL; FTRL tables start with z = 0 */
 } emb_table_desc;
+
+/* FTRL-Proximal hyperparameters (McMahan et al., KDD 2013): alpha > 0,
+ * beta, lambda1, lambda2 >= 0. */
+typedef struct {
+  float alpha;
+  float beta;
+  float lambda1;
+  float lambda2;
+} emb_ftrl_params;
 
 typedef struct {
   int64_t n_keys;
@@ -127,6 +145,7 @@ typedef struct {
   int64_t probe_bound; /* max_cluster + 1: kernels never inspect more slots per key */
   double load_factor;  /* n_keys / capacity */
   uint64_t device_bytes;
+  int64_t max_slot_keys; /* keys of the largest slot (the backward sorts rows within a slot) */
 } emb_table_stats;
 
 /*
@@ -216,6 +235,25 @@ EMB_API emb_status emb_bwd_adagrad(emb_table* table, const int64_t* offsets_d, i
                            void* workspace_d, size_t ws_bytes, void* stream);
 
 /*
+ * emb_bwd_ftrl -- the same backward with the FTRL-Proximal update instead of
+ * Adagrad (JD ads article 3.2.1 names FTRL beside Adagrad as the sparse
+ * optimizers of CTR training; the update is the per-coordinate form of
+ * McMahan et al., "Ad Click Prediction: a View from the Trenches", KDD 2013,
+ * Algorithm 1).  For each hit key and each element, with g its summed
+ * gradient and w the weight the forward read, in float32:
+ *   sigma = (sqrt(n + g*g) - sqrt(n)) / alpha;  z += g - sigma * w;  n += g*g;
+ *   w = 0 if |z| <= lambda1, else -(z - sign(z) lambda1) / ((beta + sqrt(n)) / alpha + lambda2)
+ * (half weights rounded to nearest-even; master-copy tables update the f32
+ * masters).  Rows not hit are not touched.  The table must have been created
+ * with optimizer EMB_OPT_FTRL (else EMB_ERR_INVALID_ARG); params is host
+ * memory, checked before any work is queued.  Other arguments, errors and
+ * ordering rules as emb_bwd_adagrad.
+ */
+EMB_API emb_status emb_bwd_ftrl(emb_table* table, const int64_t* offsets_d, int64_t n_bags, const int64_t* keys_d,
+                                int64_t nnz, emb_pool pool, const float* grad_out_d, const emb_ftrl_params* params,
+                                void* workspace_d, size_t ws_bytes, void* stream);
+
+/*
  * emb_bwd_phase_events -- optional timing hook (no counterpart in the pages;
  * it serves measurement).  Registers up to EMB_BWD_PHASES caller-owned
  * cudaEvent_t handles (passed as void*, created with timing enabled) that
@@ -282,6 +320,10 @@ EMB_API emb_status emb_lookup_fwd_record(emb_table* table, const int64_t* offset
 EMB_API emb_status emb_bwd_adagrad_recorded(emb_table* table, int64_t n_bags, int64_t nnz, emb_pool pool,
                                             const float* grad_out_d, float lr, float eps, void* workspace_d,
                                             size_t ws_bytes, void* stream);
+/* The recorded backward with the FTRL update of emb_bwd_ftrl. */
+EMB_API emb_status emb_bwd_ftrl_recorded(emb_table* table, int64_t n_bags, int64_t nnz, emb_pool pool,
+                                         const float* grad_out_d, const emb_ftrl_params* params, void* workspace_d,
+                                         size_t ws_bytes, void* stream);
 
 /*
  * emb_bwd_unique_keys -- the deduplicated key set of the last emb_bwd_adagrad
@@ -326,6 +368,16 @@ EMB_API emb_status emb_table_export(const emb_table* table, int64_t* keys_out, v
  */
 EMB_API emb_status emb_table_export_rows(const emb_table* table, const int64_t* ext_rows_d, int64_t n,
                                          void* values_out_d, float* acc_out_d, void* stream);
+
+/*
+ * emb_table_export_z / emb_table_import_z -- the FTRL state z of every
+ * element, f32 in keys-array order (the layout of emb_table_create's acc),
+ * host or device; the checkpoint and the resume of an FTRL table together
+ * with emb_table_export (whose accumulators are FTRL's n).  Synchronise
+ * `stream`.  EMB_ERR_INVALID_ARG on a table created for Adagrad.
+ */
+EMB_API emb_status emb_table_export_z(const emb_table* table, float* z_out, void* stream);
+EMB_API emb_status emb_table_import_z(emb_table* table, const float* z_in, void* stream);
 
 /* Copy the slot layout (key and keys-array index per slot, -1 = empty) to
  * host or device int64[capacity] buffers; either may be NULL.  Synchronises.

@@ -9,7 +9,9 @@ Pins (what ties the oracle to something other than itself) live in
 ``tests/test_oracle_pins.py``: the MurmurHash3 x64-128 verification value
 through this ``fmix64``, brute-force probe layouts on tiny tables,
 order-independence of the occupied-slot set, brute-force pooling and
-gradient sums, closed-form Adagrad and numpy's float16 rounding.
+gradient sums, closed-form Adagrad and numpy's float16 rounding; FTRL
+against torch.optim.Adagrad in the regularisation-free case it reduces to,
+and its weight against a numerical minimisation of the proximal objective.
 """
 from __future__ import annotations
 
@@ -60,6 +62,8 @@ def lib():
         L.orc_grad_free.restype = None
         L.orc_adagrad.argtypes = [_vp, ctypes.c_int64, ctypes.c_int, _vp, _vp, ctypes.c_float, ctypes.c_float]
         L.orc_f32_to_f16.argtypes = [_vp, ctypes.c_int64, _vp]
+        L.orc_ftrl.argtypes = [_vp, ctypes.c_int64, ctypes.c_int, _vp, _vp, _vp, ctypes.c_float, ctypes.c_float,
+                               ctypes.c_float, ctypes.c_float]
         _lib = L
     return _lib
 
@@ -198,3 +202,20 @@ def adagrad(G: np.ndarray, w: np.ndarray, acc: np.ndarray, lr: float, eps: float
     assert G.size == w.size == acc.size
     _check(lib().orc_adagrad(_p(G), G.size, wd, _p(w), _p(acc), ctypes.c_float(lr), ctypes.c_float(eps)))
     return w, acc
+
+
+def ftrl(G: np.ndarray, w: np.ndarray, n: np.ndarray, z: np.ndarray, alpha: float, beta: float, lambda1: float,
+         lambda2: float) -> Tuple[np.ndarray, np.ndarray, np.ndarray]:
+    """Element-wise FTRL-Proximal on copies of (w, n, z); w float32 or float16.
+    Returns (w', n', z')."""
+    G = np.ascontiguousarray(G, dtype=np.float64)
+    w = np.array(w, copy=True)
+    n = np.array(n, dtype=np.float32, copy=True)
+    z = np.array(z, dtype=np.float32, copy=True)
+    wd = 1 if w.dtype == np.float16 else 0
+    if wd == 0:
+        w = w.astype(np.float32)
+    assert G.size == w.size == n.size == z.size
+    _check(lib().orc_ftrl(_p(G), G.size, wd, _p(w), _p(n), _p(z), ctypes.c_float(alpha), ctypes.c_float(beta),
+                          ctypes.c_float(lambda1), ctypes.c_float(lambda2)))
+    return w, n, z

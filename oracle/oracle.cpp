@@ -344,6 +344,47 @@ int orc_adagrad(const double* G, int64_t n, int wdtype, void* w, float* acc, flo
   return ORC_OK;
 }
 
+// FTRL-Proximal, per coordinate (McMahan et al., "Ad Click Prediction: a View
+// from the Trenches", KDD 2013, Algorithm 1; the JD article 3.2.1 names FTRL as
+// the other sparse optimizer of CTR training).  For each element, with the
+// weight w the forward used and the state (z, n), float32 arithmetic in this
+// order:
+//   g = (float)G;  n' = n + g*g;  sigma = (sqrt(n') - sqrt(n)) / alpha;
+//   z' = (z + g) - sigma * w;
+//   w' = 0 if |z'| <= lambda1, else -((z' - sign(z') lambda1) / ((beta + sqrt(n')) / alpha + lambda2)).
+// Half weights are read exactly and the result rounded to half (RNE).
+int orc_ftrl(const double* G, int64_t n, int wdtype, void* w, float* nacc, float* z, float alpha, float beta,
+             float l1, float l2) {
+  for (int64_t i = 0; i < n; ++i) {
+    float g = (float)G[i];
+    float wv = (wdtype == 1) ? (float)((_Float16*)w)[i] : ((float*)w)[i];
+    float n0 = nacc[i];
+    float gg = g * g;
+    float n1 = n0 + gg;
+    float sn = std::sqrt(n0);
+    float sn1 = std::sqrt(n1);
+    float sigma = (sn1 - sn) / alpha;
+    float zs = z[i] + g;
+    float sw = sigma * wv;
+    float z1 = zs - sw;
+    float nw;
+    if (std::fabs(z1) <= l1) {
+      nw = 0.0f;
+    } else {
+      float num = z1 - (z1 > 0.0f ? l1 : -l1);
+      float den = (beta + sn1) / alpha + l2;
+      nw = -(num / den);
+    }
+    nacc[i] = n1;
+    z[i] = z1;
+    if (wdtype == 1)
+      ((_Float16*)w)[i] = (_Float16)nw;
+    else
+      ((float*)w)[i] = nw;
+  }
+  return ORC_OK;
+}
+
 // float -> half, IEEE round-to-nearest-even (the oracle's writeback rounding).
 int orc_f32_to_f16(const float* x, int64_t n, uint16_t* out) {
   for (int64_t i = 0; i < n; ++i) {

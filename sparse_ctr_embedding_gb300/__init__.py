@@ -22,6 +22,7 @@ __all__ = [
     "EmbError", "LibraryNotBuilt", "Table", "lib", "declared_symbols",
     "emb_table_create", "emb_table_destroy", "emb_table_get_stats", "emb_table_plan",
     "emb_lookup_fwd", "emb_lookup_fwd_record", "emb_bwd_adagrad_recorded", "emb_bwd_workspace_size", "emb_bwd_adagrad", "emb_bwd_adagrad_noalloc",
+    "emb_bwd_ftrl", "emb_bwd_ftrl_recorded", "emb_table_export_z", "emb_table_import_z",
     "emb_bwd_unique_keys", "emb_bwd_phase_events", "EMB_NOALLOC_SCRATCH_BYTES", "EMB_SORT_DIGIT_BITS", "BWD_PHASES",
     "emb_resolve", "emb_table_export", "emb_table_export_rows", "emb_table_slots", "emb_check_device_flag",
     "emb_status_string", "emb_last_error",
@@ -38,6 +39,7 @@ EMB_SORT_DIGIT_BITS = 7
 BWD_PHASES = ("expand", "sort", "reduce", "fixup")
 _DTYPE = {"f32": 0, "f16": 1, "f16m": 2}   # f16m: f32 master rows + the f16 copy the forward reads
 _POOL = {"sum": 0, "mean": 1}
+_OPT = {"adagrad": 0, "ftrl": 1}
 
 
 class LibraryNotBuilt(ImportError):
@@ -54,7 +56,13 @@ class EmbError(RuntimeError):
 
 class _Desc(ctypes.Structure):
     _fields_ = [("n_slots", ctypes.c_int32), ("slot_dim", ctypes.POINTER(ctypes.c_int32)),
-                ("wdtype", ctypes.c_int), ("capacity", ctypes.c_int64), ("acc_init", ctypes.c_float)]
+                ("wdtype", ctypes.c_int), ("capacity", ctypes.c_int64), ("acc_init", ctypes.c_float),
+                ("optimizer", ctypes.c_int)]
+
+
+class _Ftrl(ctypes.Structure):
+    _fields_ = [("alpha", ctypes.c_float), ("beta", ctypes.c_float), ("lambda1", ctypes.c_float),
+                ("lambda2", ctypes.c_float)]
 
 
 class _Stats(ctypes.Structure):
@@ -62,7 +70,8 @@ class _Stats(ctypes.Structure):
                 ("n_slots", ctypes.c_int32), ("sum_dims", ctypes.c_int32), ("max_dim", ctypes.c_int32),
                 ("wdtype", ctypes.c_int32), ("max_probe", ctypes.c_int64), ("sum_probe", ctypes.c_int64),
                 ("max_cluster", ctypes.c_int64), ("probe_bound", ctypes.c_int64),
-                ("load_factor", ctypes.c_double), ("device_bytes", ctypes.c_uint64)]
+                ("load_factor", ctypes.c_double), ("device_bytes", ctypes.c_uint64),
+                ("max_slot_keys", ctypes.c_int64)]
 
     def as_dict(self):
         return {f: getattr(self, f) for f, _ in self._fields_}
@@ -96,6 +105,12 @@ def lib():
                                          ctypes.c_size_t, _vp],
             "emb_bwd_adagrad_noalloc": [_vp, _vp, _i64, _vp, _i64, ctypes.c_int, _vp, ctypes.c_float,
                                         ctypes.c_float, _vp],
+            "emb_bwd_ftrl": [_vp, _vp, _i64, _vp, _i64, ctypes.c_int, _vp, ctypes.POINTER(_Ftrl), _vp,
+                             ctypes.c_size_t, _vp],
+            "emb_bwd_ftrl_recorded": [_vp, _i64, _i64, ctypes.c_int, _vp, ctypes.POINTER(_Ftrl), _vp,
+                                      ctypes.c_size_t, _vp],
+            "emb_table_export_z": [_vp, _vp, _vp],
+            "emb_table_import_z": [_vp, _vp, _vp],
             "emb_resolve": [_vp, _vp, _i64, _vp, _vp, _vp],
             "emb_table_export": [_vp, _vp, _vp, _vp, _vp],
             "emb_table_slots": [_vp, _vp, _vp, _vp],
@@ -157,19 +172,20 @@ def _cuda(t: torch.Tensor, dtype, name):
     return _ptr(t, dtype, name)
 
 
-def _desc(dims, wdtype, capacity, acc_init):
+def _desc(dims, wdtype, capacity, acc_init, optimizer="adagrad"):
     dims_arr = (ctypes.c_int32 * len(dims))(*[int(d) for d in dims])
-    d = _Desc(len(dims), dims_arr, _DTYPE[wdtype], int(capacity), float(acc_init))
+    d = _Desc(len(dims), dims_arr, _DTYPE[wdtype], int(capacity), float(acc_init), _OPT[optimizer])
     return d, dims_arr
 
 
 class Table:
     """Owner of one emb_table handle."""
 
-    def __init__(self, handle: int, dims, wdtype: str):
+    def __init__(self, handle: int, dims, wdtype: str, optimizer: str = "adagrad"):
         self._h = _vp(handle)
         self.dims = tuple(int(d) for d in dims)
         self.wdtype = wdtype
+        self.optimizer = optimizer
         self.stats = emb_table_get_stats(self)
 
     @property
@@ -194,17 +210,18 @@ class Table:
 
 def emb_table_create(dims, wdtype: str, keys: torch.Tensor, values: Optional[torch.Tensor] = None,
                      acc: Optional[torch.Tensor] = None, capacity: int = 0, acc_init: float = 0.0,
-                     stream=None) -> Table:
-    """keys: CPU int64; values/acc: CPU or CUDA, ragged rows in keys order."""
+                     stream=None, optimizer: str = "adagrad") -> Table:
+    """keys: CPU int64; values/acc: CPU or CUDA, ragged rows in keys order.
+    optimizer: "adagrad" or "ftrl" (acc is then FTRL's n; z starts at 0)."""
     if keys.is_cuda:
         raise ValueError("keys must be host memory (the table is prepared on the host)")
     wt = torch.float16 if wdtype == "f16" else torch.float32
-    d, _keep = _desc(dims, wdtype, capacity, acc_init)
+    d, _keep = _desc(dims, wdtype, capacity, acc_init, optimizer)
     h = _vp()
     _check(lib().emb_table_create(ctypes.byref(d), _ptr(keys, torch.int64, "keys"), keys.numel(),
                                   _ptr(values, wt, "values"), _ptr(acc, torch.float32, "acc"), _stream(stream),
                                   ctypes.byref(h)))
-    return Table(h.value, dims, wdtype)
+    return Table(h.value, dims, wdtype, optimizer)
 
 
 def emb_table_destroy(table: Table):
@@ -293,6 +310,39 @@ def emb_bwd_adagrad_noalloc(table: Table, offsets: torch.Tensor, keys: torch.Ten
                                          _cuda(keys, torch.int64, "keys"), keys.numel(), _POOL[pool],
                                          _cuda(grad_out, torch.float32, "grad_out"), ctypes.c_float(lr),
                                          ctypes.c_float(eps), _stream(stream)))
+
+
+def _ftrl(alpha, beta, lambda1, lambda2):
+    return _Ftrl(float(alpha), float(beta), float(lambda1), float(lambda2))
+
+
+def emb_bwd_ftrl(table: Table, offsets: torch.Tensor, keys: torch.Tensor, pool: str, grad_out: torch.Tensor,
+                 alpha: float, beta: float, lambda1: float, lambda2: float, workspace: torch.Tensor,
+                 stream=None) -> None:
+    """The backward with the FTRL-Proximal update (tables created with optimizer="ftrl")."""
+    p = _ftrl(alpha, beta, lambda1, lambda2)
+    _check(lib().emb_bwd_ftrl(table.handle, _cuda(offsets, torch.int64, "offsets"), offsets.numel() - 1,
+                              _cuda(keys, torch.int64, "keys"), keys.numel(), _POOL[pool],
+                              _cuda(grad_out, torch.float32, "grad_out"), ctypes.byref(p),
+                              _cuda(workspace, None, "workspace"), workspace.numel() * workspace.element_size(),
+                              _stream(stream)))
+
+
+def emb_bwd_ftrl_recorded(table: Table, n_bags: int, nnz: int, pool: str, grad_out: torch.Tensor, alpha: float,
+                          beta: float, lambda1: float, lambda2: float, workspace: torch.Tensor, stream=None) -> None:
+    p = _ftrl(alpha, beta, lambda1, lambda2)
+    _check(lib().emb_bwd_ftrl_recorded(table.handle, n_bags, nnz, _POOL[pool],
+                                       _cuda(grad_out, torch.float32, "grad_out"), ctypes.byref(p),
+                                       _cuda(workspace, None, "workspace"),
+                                       workspace.numel() * workspace.element_size(), _stream(stream)))
+
+
+def emb_table_export_z(table: Table, z_out: torch.Tensor, stream=None) -> None:
+    _check(lib().emb_table_export_z(table.handle, _ptr(z_out, torch.float32, "z_out"), _stream(stream)))
+
+
+def emb_table_import_z(table: Table, z_in: torch.Tensor, stream=None) -> None:
+    _check(lib().emb_table_import_z(table.handle, _ptr(z_in, torch.float32, "z_in"), _stream(stream)))
 
 
 def emb_bwd_phase_events(table: Table, events) -> None:

@@ -48,7 +48,7 @@ emb_status check_batch(const emb_table* t, const int64_t* offsets_d, int64_t n_b
                        int64_t nnz, int pool);
 cudaError_t launch_forward(const emb_table* t, const long long* offsets, long long n_bags, const long long* keys,
                            long long nnz, int mean, float* out, unsigned* K, unsigned* V, float* scale,
-                           unsigned long long* work, cudaStream_t st);
+                           const unsigned* dest, unsigned long long* work, cudaStream_t st);
 
 constexpr int kChunk = 256;                      // sorted positions per reduce sub-chunk
 constexpr int kSortWarps = 8;
@@ -68,27 +68,42 @@ struct WsHeader {
   unsigned magic;
   unsigned nnz;
   unsigned n_bags;
-  unsigned sorted_in_b;  // 1: sorted pairs are in buffer B
-  unsigned miss_row;     // sentinel row of a miss (= n_rows)
-  unsigned n_unique;     // filled by emb_bwd_unique_keys
+  unsigned sorted_in_b;      // 1: sorted pairs are in buffer B
+  unsigned miss_row;         // sentinel row of a miss (= n_rows)
+  unsigned n_unique;         // filled by emb_bwd_unique_keys
+  unsigned long long total;  // sum of the (clamped) bag lengths: nnz unless the offsets are malformed
+};
+
+// One region of the sort: the pairs of one feature slot, or (the last region)
+// pairs that are made absent.  Regions tile the positions [0, nnz) in order.
+struct SortSeg {
+  unsigned lo, hi;  // positions [lo, hi)
+  unsigned tile0;   // first sort tile of the region (the entry after the last region: the tile count)
+  unsigned rbase;   // first internal row of the slot
+  unsigned cap;     // rows of the slot: in-slot row numbers are clamped to it, so misses sort last
+  unsigned absent;  // 1: the first sort pass turns every pair of the region into an absent pair
+  unsigned pad0, pad1;
 };
 
 static size_t align_up(size_t x) { return (x + 255) & ~(size_t)255; }
 
 struct WsLayout {
-  size_t hdr, kA, kB, vA, vB, scale, counts, partials, partA, partB, arow, zero, work, fwork, uniq, total;
-  unsigned n_tiles_sort, n_chunks, n_scan_partials;
+  size_t hdr, kA, kB, vA, vB, scale, dest, sseg, counts, partials, partA, partB, arow, zero, work, fwork, uniq, total;
+  unsigned n_tiles_sort, n_regions, n_chunks, n_scan_partials;
   int max_dim;
 };
 
 static WsLayout ws_layout(const emb_table* t, long long n_bags, long long nnz) {
   WsLayout L{};
   const size_t n = (size_t)std::max<long long>(nnz, 1);
+  const size_t nb = (size_t)std::max<long long>(n_bags, 1);
   L.max_dim = t->st.max_dim;
-  L.n_tiles_sort = (unsigned)((n + kSortTile - 1) / kSortTile);
+  L.n_regions = (unsigned)t->st.n_slots + 1;  // one per slot, then the absent region
+  // every region adds at most one partial tile
+  L.n_tiles_sort = (unsigned)((n + kSortTile - 1) / kSortTile) + L.n_regions;
   L.n_chunks = (unsigned)((n + kChunk - 1) / kChunk);
   const size_t n_counts = (size_t)kDigits * L.n_tiles_sort;
-  const size_t scan_n = std::max(n_counts, n);
+  const size_t scan_n = std::max(std::max(n_counts, n), nb);
   L.n_scan_partials = (unsigned)((scan_n + kScanTile - 1) / kScanTile);
   size_t o = 0;
   auto take = [&](size_t bytes) {
@@ -101,7 +116,9 @@ static WsLayout ws_layout(const emb_table* t, long long n_bags, long long nnz) {
   L.kB = take(n * 4);
   L.vA = take(n * 4);
   L.vB = take(n * 4);
-  L.scale = take((size_t)std::max<long long>(n_bags, 1) * 4);
+  L.scale = take(nb * 4);
+  L.dest = take(nb * 4);                                  // first position of each bag's pairs
+  L.sseg = take((size_t)(L.n_regions + 1) * sizeof(SortSeg));
   L.counts = take(n_counts * 4);
   L.partials = take((size_t)(L.n_scan_partials + 1) * 4);
   L.partA = take((size_t)L.n_chunks * L.max_dim * 4);
@@ -123,49 +140,19 @@ __device__ __forceinline__ unsigned lanemask_lt() {
 
 // ------------------------------------------------------------------ 1. expand
 
-// Header of a recording forward, launched before it with one block.  With
-// malformed (flagged) offsets some positions lie outside every bag: before
-// the first offset or at or after the last one (clamped to [0, nnz]; between
-// them every position is inside some bag).  They are written here as absent
-// pairs (row n_rows, bag n_bags), so no later kernel reads a stale pair; the
-// forward that follows overwrites every position that is inside a bag.
-__global__ void ws_header_kernel(WsHeader* hdr, unsigned nnz, unsigned n_bags, unsigned sorted_in_b, unsigned miss,
-                                 const long long* __restrict__ offsets, unsigned* __restrict__ K,
-                                 unsigned* __restrict__ V) {
-  if (threadIdx.x == 0) {
-    hdr->magic = kMagic;
-    hdr->nnz = nnz;
-    hdr->n_bags = n_bags;
-    hdr->sorted_in_b = sorted_in_b;
-    hdr->miss_row = miss;
-    hdr->n_unique = 0;
-  }
-  // no bags: every position is outside
-  const long long lo = n_bags == 0 ? (long long)nnz : min(max(offsets[0], 0LL), (long long)nnz);
-  const long long hi = n_bags == 0 ? (long long)nnz : min(max(offsets[n_bags], 0LL), (long long)nnz);
-  for (long long i = threadIdx.x; i < lo; i += blockDim.x) { K[i] = miss; V[i] = n_bags; }
-  for (long long i = hi + threadIdx.x; i < (long long)nnz; i += blockDim.x) { K[i] = miss; V[i] = n_bags; }
-}
-
+// Unrecorded path: one warp per bag probes its keys and writes the pair
+// (internal row, bag) of every occurrence at the bag's place in the slot-major
+// order (dest[bag], see placement below; row n_rows for a miss, which sorts last
+// in its slot), and 1/L per bag for mean.
 __global__ void __launch_bounds__(256) expand_kernel(TableView t, const long long* __restrict__ offsets,
                                                      long long n_bags, const long long* __restrict__ keys,
-                                                     long long nnz, int mean, unsigned* __restrict__ K,
-                                                     unsigned* __restrict__ V, float* __restrict__ scale,
-                                                     WsHeader* hdr, unsigned sorted_in_b) {
+                                                     long long nnz, int mean, const unsigned* __restrict__ dest,
+                                                     unsigned* __restrict__ K, unsigned* __restrict__ V,
+                                                     float* __restrict__ scale) {
   const int lane = threadIdx.x & 31;
   const long long gw = (blockIdx.x * (long long)blockDim.x + threadIdx.x) >> 5;
-  if (gw == 0 && lane == 0) {
-    hdr->magic = kMagic;
-    hdr->nnz = (unsigned)nnz;
-    hdr->n_bags = (unsigned)n_bags;
-    hdr->sorted_in_b = sorted_in_b;
-    hdr->miss_row = t.n_rows;
-    hdr->n_unique = 0;
-  }
   const long long nwarps = ((long long)gridDim.x * blockDim.x) >> 5;
   const unsigned S = (unsigned)t.n_slots;
-  if (n_bags == 0 && gw == 0)  // no bags: every position is absent
-    for (long long i = lane; i < nnz; i += 32) { K[i] = t.n_rows; V[i] = 0u; }
   for (long long bag = gw; bag < n_bags; bag += nwarps) {
     const int s = (int)((unsigned)bag % S);
     long long start = offsets[bag], end = offsets[bag + 1];
@@ -175,13 +162,7 @@ __global__ void __launch_bounds__(256) expand_kernel(TableView t, const long lon
       end = min(max(end, start), nnz);
     }
     if (mean && lane == 0) scale[bag] = end > start ? 1.0f / (float)(end - start) : 0.f;
-    // with malformed (flagged) offsets, positions before the first bag or after
-    // the last one belong to no bag: they become absent pairs, so no later
-    // kernel reads a stale pair
-    if (bag == 0)
-      for (long long i = lane; i < start; i += 32) { K[i] = t.n_rows; V[i] = (unsigned)n_bags; }
-    if (bag == n_bags - 1)
-      for (long long i = end + lane; i < nnz; i += 32) { K[i] = t.n_rows; V[i] = (unsigned)n_bags; }
+    const long long d0 = (long long)dest[bag] - start;
     for (long long i = start + lane; i < end; i += 32) {
       const long long k = keys[i];
       unsigned row = t.n_rows, ext;
@@ -191,8 +172,11 @@ __global__ void __launch_bounds__(256) expand_kernel(TableView t, const long lon
       } else if (!probe(t, k, &row, &ext, &h)) {
         row = t.n_rows;
       }
-      K[i] = row;
-      V[i] = (unsigned)bag;
+      const long long p = d0 + i;  // inside [0, nnz) unless the offsets are malformed
+      if (p < nnz) {
+        K[p] = row;
+        V[p] = (unsigned)bag;
+      }
     }
   }
 }
@@ -229,20 +213,55 @@ __device__ __forceinline__ void warp_rank(unsigned (&d)[kSortItems], unsigned (&
   }
 }
 
-// Digit counts of one tile (the same kSortTile keys the scatter kernel ranks).
-// Each thread takes kSortItems consecutive keys and adds whole runs of equal
+// The sort region of a tile: the largest r < n_regions with sg[r].tile0 <=
+// tile, or n_regions for the spare tiles past the last region (the launch
+// covers the most tiles any placement can need).
+__device__ __forceinline__ unsigned region_of_tile(const SortSeg* __restrict__ sg, unsigned n_regions, unsigned tile) {
+  if (tile >= sg[n_regions].tile0) return n_regions;
+  unsigned lo = 0, hi = n_regions - 1;
+  while (lo < hi) {
+    const unsigned mid = (lo + hi + 1) >> 1;
+    if (sg[mid].tile0 <= tile) lo = mid; else hi = mid - 1;
+  }
+  return lo;
+}
+
+// Digit of a row in its region: of the in-slot row number, clamped to the
+// slot's row count so that misses (row n_rows) sort last; 0 in the absent region.
+__device__ __forceinline__ unsigned region_digit(const SortSeg& g, unsigned k, int shift) {
+  if (g.absent) return 0u;
+  const unsigned in_slot = min(k - g.rbase, g.cap);  // k < rbase wraps high and clamps too
+  return (in_slot >> shift) & (kDigits - 1);
+}
+
+// Digit counts of one tile of one region (the same keys the scatter kernel
+// ranks), laid out region by region, digit-major within a region, so that
+// one exclusive scan of the whole array gives every (tile, digit) its first
+// output position and each region's output stays inside the region.  Each
+// thread takes kSortItems consecutive keys and adds whole runs of equal
 // digits with one shared atomic (sorted passes and hot rows give long runs).
-__global__ void __launch_bounds__(kSortThreads) radix_count_kernel(const unsigned* __restrict__ keys, unsigned n,
-                                                                   int shift, unsigned* __restrict__ counts,
-                                                                   unsigned n_tiles) {
+__global__ void __launch_bounds__(kSortThreads) radix_count_kernel(const unsigned* __restrict__ keys,
+                                                                   const SortSeg* __restrict__ sg,
+                                                                   unsigned n_regions, int shift,
+                                                                   unsigned* __restrict__ counts) {
   __shared__ unsigned cnt[kSortWarps][kDigits];
+  __shared__ unsigned reg;
   const int w = threadIdx.x >> 5;
+  const unsigned tile = blockIdx.x;
+  if (threadIdx.x == 0) reg = region_of_tile(sg, n_regions, tile);
   for (int i = threadIdx.x; i < kSortWarps * kDigits; i += kSortThreads) (&cnt[0][0])[i] = 0;
   __syncthreads();
-  const unsigned tile = blockIdx.x;
-  const unsigned base = tile * kSortTile + threadIdx.x * kSortItems;
+  const unsigned r = reg;
+  if (r == n_regions) {  // a spare tile: zero counts in its own slice, after every region's
+    for (int dg = threadIdx.x; dg < kDigits; dg += kSortThreads) counts[(size_t)kDigits * tile + dg] = 0;
+    return;
+  }
+  const SortSeg g = sg[r];
+  const unsigned nt = sg[r + 1].tile0 - g.tile0, lt = tile - g.tile0;
+  const unsigned lo = g.lo + lt * kSortTile, hi = min(lo + kSortTile, g.hi);
+  const unsigned base = lo + threadIdx.x * kSortItems;
   unsigned k[kSortItems];
-  if (base + kSortItems <= n) {
+  if ((lo & 3u) == 0 && base + kSortItems <= hi) {
     const uint4* p = reinterpret_cast<const uint4*>(keys + base);
 #pragma unroll
     for (int q = 0; q < kSortItems / 4; ++q) {
@@ -251,14 +270,14 @@ __global__ void __launch_bounds__(kSortThreads) radix_count_kernel(const unsigne
     }
   } else {
 #pragma unroll
-    for (int j = 0; j < kSortItems; ++j) k[j] = base + j < n ? keys[base + j] : 0u;
+    for (int j = 0; j < kSortItems; ++j) k[j] = base + j < hi ? keys[base + j] : 0u;
   }
-  const int m = base >= n ? 0 : (int)min((unsigned)kSortItems, n - base);
+  const int m = base >= hi ? 0 : (int)min((unsigned)kSortItems, hi - base);
   unsigned cur = 0, run = 0;
 #pragma unroll
   for (int j = 0; j < kSortItems; ++j) {
     if (j < m) {
-      const unsigned dg = (k[j] >> shift) & (kDigits - 1);
+      const unsigned dg = region_digit(g, k[j], shift);
       if (run && dg != cur) {
         atomicAdd(&cnt[w][cur], run);
         run = 0;
@@ -273,7 +292,7 @@ __global__ void __launch_bounds__(kSortThreads) radix_count_kernel(const unsigne
     unsigned tot = 0;
 #pragma unroll
     for (int ww = 0; ww < kSortWarps; ++ww) tot += cnt[ww][dg];
-    counts[(size_t)dg * n_tiles + tile] = tot;
+    counts[(size_t)kDigits * g.tile0 + (size_t)dg * nt + lt] = tot;
   }
 }
 
@@ -306,9 +325,12 @@ __device__ __forceinline__ unsigned block_excl_scan(unsigned v, unsigned* sm) {
   return sm[w] + x - v;
 }
 
+// Stable scatter of one tile of one region by digit.  In the absent region
+// every pair becomes (miss row, n_bags) as it is loaded.
 __global__ void __launch_bounds__(kSortThreads, 3) radix_scatter_kernel(
     const unsigned* __restrict__ kin, const unsigned* __restrict__ vin, unsigned* __restrict__ kout,
-    unsigned* __restrict__ vout, unsigned n, int shift, const unsigned* __restrict__ counts, unsigned n_tiles) {
+    unsigned* __restrict__ vout, int shift, const unsigned* __restrict__ counts, const SortSeg* __restrict__ sg,
+    unsigned n_regions, unsigned miss, unsigned n_bags) {
   extern __shared__ unsigned smem[];
   unsigned(*cnt)[kDigits] = reinterpret_cast<unsigned(*)[kDigits]>(smem);  // [kSortWarps][kDigits]
   unsigned* gbase = smem + kSortWarps * kDigits;                             // [kDigits]
@@ -316,21 +338,30 @@ __global__ void __launch_bounds__(kSortThreads, 3) radix_scatter_kernel(
   unsigned* wtot = bstart + kDigits;                                          // [33]
   unsigned* tk = wtot + 33;                                                   // [kSortTile]
   unsigned* tv = tk + kSortTile;                                              // [kSortTile]
+  __shared__ unsigned reg;
   const int w = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const unsigned tile = blockIdx.x;
-  for (int i = threadIdx.x; i < kSortWarps * kDigits; i += kSortThreads) smem[i] = 0;
-  for (int dg = threadIdx.x; dg < kDigits; dg += kSortThreads) gbase[dg] = counts[(size_t)dg * n_tiles + tile];
+  if (threadIdx.x == 0) reg = region_of_tile(sg, n_regions, tile);
   __syncthreads();
-  const unsigned base = tile * kSortTile + w * 32 * kSortItems;
+  const unsigned r = reg;
+  if (r == n_regions) return;  // a spare tile
+  const SortSeg g = sg[r];
+  const unsigned nt = sg[r + 1].tile0 - g.tile0, lt = tile - g.tile0;
+  const unsigned lo = g.lo + lt * kSortTile, hi = min(lo + kSortTile, g.hi);
+  for (int i = threadIdx.x; i < kSortWarps * kDigits; i += kSortThreads) smem[i] = 0;
+  for (int dg = threadIdx.x; dg < kDigits; dg += kSortThreads)
+    gbase[dg] = counts[(size_t)kDigits * g.tile0 + (size_t)dg * nt + lt];
+  __syncthreads();
+  const unsigned base = lo + w * 32 * kSortItems;
   unsigned k[kSortItems], v[kSortItems], d[kSortItems], rank[kSortItems];
   bool valid[kSortItems];
 #pragma unroll
-  for (int r = 0; r < kSortItems; ++r) {
-    const unsigned i = base + r * 32 + lane;
-    valid[r] = i < n;
-    k[r] = valid[r] ? kin[i] : 0;
-    v[r] = valid[r] ? vin[i] : 0;
-    d[r] = (k[r] >> shift) & (kDigits - 1);
+  for (int q = 0; q < kSortItems; ++q) {
+    const unsigned i = base + q * 32 + lane;
+    valid[q] = i < hi;
+    k[q] = valid[q] ? (g.absent ? miss : kin[i]) : 0;
+    v[q] = valid[q] ? (g.absent ? n_bags : vin[i]) : 0;
+    d[q] = region_digit(g, k[q], shift);
   }
   warp_rank(d, rank, valid, cnt[w]);
   __syncthreads();
@@ -368,18 +399,18 @@ __global__ void __launch_bounds__(kSortThreads, 3) radix_scatter_kernel(
   }
   __syncthreads();
 #pragma unroll
-  for (int r = 0; r < kSortItems; ++r) {
-    if (valid[r]) {
-      const unsigned pos = cnt[w][d[r]] + rank[r];
-      tk[pos] = k[r];
-      tv[pos] = v[r];
+  for (int q = 0; q < kSortItems; ++q) {
+    if (valid[q]) {
+      const unsigned pos = cnt[w][d[q]] + rank[q];
+      tk[pos] = k[q];
+      tv[pos] = v[q];
     }
   }
   __syncthreads();
-  const unsigned tile_n = min((unsigned)kSortTile, n - tile * kSortTile);
+  const unsigned tile_n = hi - lo;
   for (unsigned j = threadIdx.x; j < tile_n; j += kSortThreads) {
     const unsigned kk = tk[j];
-    const unsigned dg = (kk >> shift) & (kDigits - 1);
+    const unsigned dg = region_digit(g, kk, shift);
     const unsigned gp = gbase[dg] + (j - bstart[dg]);
     kout[gp] = kk;
     vout[gp] = tv[j];
@@ -459,6 +490,128 @@ __global__ void __launch_bounds__(kScanThreads) scan_down_kernel(const unsigned*
   }
 }
 
+// ------------------------------------------------------------------ placement of the pairs
+//
+// The pair of every occurrence is written straight into the region of its
+// feature slot, in slot-major order: the bags of slot 0 (b ascending), then
+// those of slot 1, and so on; within a bag, in key order.  Rows are numbered
+// slot-major, so the stable sort then only orders each slot's in-slot row
+// numbers: at 64 slots of 1.56M keys 21 bits (3 passes of 7) instead of 27
+// (4 passes), and the occurrences of a row keep the order they had before
+// (the bags of its slot in b order), so the per-row sums are unchanged.
+// dest[bag] is the exclusive prefix sum, in slot-major order (t = s * B + b),
+// of the bag lengths, each clamped exactly as the forward clamps malformed
+// offsets; it is stored by bag (b * S + s), the order the forward walks.
+
+__device__ __forceinline__ unsigned long long bag_len_t(const long long* __restrict__ offsets, size_t t,
+                                                        unsigned long long B, unsigned S, long long nnz) {
+  const unsigned long long s = t / B, b = t % B;
+  const unsigned long long bag = b * S + s;
+  const long long start = min(max(offsets[bag], 0LL), nnz);
+  const long long end = min(max(offsets[bag + 1], start), nnz);
+  return (unsigned long long)(end - start);
+}
+
+// Per-tile sums of the slot-major bag lengths (strided like scan_reduce_kernel),
+// and their exact 64-bit total in the header (zeroed beforehand): it equals
+// nnz exactly when the clamped bags tile [0, nnz).
+__global__ void __launch_bounds__(kScanThreads) len_scan_reduce_kernel(const long long* __restrict__ offsets,
+                                                                       unsigned long long B, unsigned S,
+                                                                       long long nnz, size_t n,
+                                                                       unsigned* __restrict__ partials,
+                                                                       WsHeader* hdr) {
+  __shared__ unsigned wt[33];
+  const size_t base = (size_t)blockIdx.x * kScanTile;
+  unsigned long long s64 = 0;
+#pragma unroll 4
+  for (int j = 0; j < kScanItems; ++j) {
+    const size_t i = base + (size_t)j * kScanThreads + threadIdx.x;
+    if (i < n) s64 += bag_len_t(offsets, i, B, S, nnz);
+  }
+  block_excl_scan((unsigned)s64, wt);
+  if (threadIdx.x == 0) partials[blockIdx.x] = wt[32];
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) s64 += __shfl_xor_sync(0xffffffffu, s64, o);
+  if ((threadIdx.x & 31) == 0 && s64) atomicAdd(&hdr->total, s64);
+}
+
+// dest[bag of t] = exclusive prefix of the slot-major bag lengths (blocked, like scan_down_kernel).
+__global__ void __launch_bounds__(kScanThreads) len_scan_down_kernel(const long long* __restrict__ offsets,
+                                                                     unsigned long long B, unsigned S, long long nnz,
+                                                                     size_t n, unsigned* __restrict__ dest,
+                                                                     const unsigned* __restrict__ partials) {
+  __shared__ unsigned wt[33];
+  const size_t base = (size_t)blockIdx.x * kScanTile + (size_t)threadIdx.x * kScanItems;
+  unsigned v[kScanItems];
+  unsigned s = 0;
+#pragma unroll
+  for (int j = 0; j < kScanItems; ++j) {
+    v[j] = base + j < n ? (unsigned)bag_len_t(offsets, base + j, B, S, nnz) : 0u;
+    s += v[j];
+  }
+  unsigned excl = block_excl_scan(s, wt) + partials[blockIdx.x];
+#pragma unroll
+  for (int j = 0; j < kScanItems; ++j) {
+    if (base + j < n) dest[((base + j) % B) * S + (base + j) / B] = excl;
+    excl += v[j];
+  }
+}
+
+// One block: the workspace header and the sort regions.  Region s < S holds
+// slot s's pairs, from the first position of its first bag (bag s, sample 0)
+// to that of slot s + 1 (the last slot ends at nnz); region S, the absent
+// region, is empty.  If the clamped bag lengths do not add up to nnz
+// (malformed offsets; flagged) the bags do not tile [0, nnz): then every
+// slot region is empty and the absent region covers all of [0, nnz), so the
+// first sort pass overwrites every position with an absent pair and the
+// backward updates nothing.
+__global__ void __launch_bounds__(1024) seg_setup_kernel(TableView t, WsHeader* hdr, unsigned nnz,
+                                                         unsigned long long n_bags, unsigned sorted_in_b,
+                                                         const unsigned* __restrict__ dest, SortSeg* __restrict__ sg) {
+  __shared__ unsigned wt[33];
+  __shared__ unsigned carry;
+  const unsigned S = (unsigned)t.n_slots;
+  const unsigned long long B = n_bags / S;
+  const bool placed = B > 0 && hdr->total == (unsigned long long)nnz;
+  if (threadIdx.x == 0) {
+    hdr->magic = kMagic;
+    hdr->nnz = nnz;
+    hdr->n_bags = (unsigned)n_bags;
+    hdr->sorted_in_b = sorted_in_b;
+    hdr->miss_row = t.n_rows;
+    hdr->n_unique = 0;
+    carry = 0;
+    if (!placed && nnz > 0) atomicOr(t.flags, EMB_FLAG_BAD_OFFSETS);
+  }
+  __syncthreads();
+  for (unsigned r0 = 0; r0 <= S; r0 += blockDim.x) {
+    const unsigned r = r0 + threadIdx.x;
+    SortSeg g{0u, 0u, 0u, 0u, 0u, 0u, 0u, 0u};
+    unsigned nt = 0;
+    if (r < S) {
+      if (placed) {
+        g.lo = dest[r];
+        g.hi = r + 1 < S ? dest[r + 1] : nnz;
+      }
+      const SlotInfo si = t.sinfo[r];
+      g.rbase = si.row_base;
+      g.cap = si.n_rows;
+    } else if (r == S) {
+      g.lo = placed ? nnz : 0u;
+      g.hi = nnz;
+      g.absent = 1;
+    }
+    if (r <= S) nt = (g.hi - g.lo + kSortTile - 1) / kSortTile;
+    const unsigned ex = block_excl_scan(nt, wt);
+    g.tile0 = carry + ex;
+    if (r <= S) sg[r] = g;
+    __syncthreads();
+    if (threadIdx.x == 0) carry += wt[32];
+    __syncthreads();
+  }
+  if (threadIdx.x == 0) sg[S + 1].tile0 = carry;  // tile count
+}
+
 // ------------------------------------------------------------------ 3. reduce + Adagrad
 
 // Four consecutive weights as float (one 16-byte f32 or 8-byte f16 access).
@@ -488,35 +641,86 @@ __device__ __forceinline__ void stw4(__half* p, const float (&v)[4]) {
   __stcs(reinterpret_cast<uint2*>(p), x);
 }
 
-// One element of the Adagrad update:  acc += g*g;  w -= lr*g / (sqrt(acc) + eps).
+// ------------------------------------------------------------------ optimizers
+//
+// The update every element of a hit row receives, given its summed gradient g.
+
+// Adagrad (JD ads article 3.2.1):  acc += g*g;  w -= lr*g / (sqrt(acc) + eps).
 // sqrt(acc) is acc * rsqrt(acc) and the quotient a fast divide (hardware
 // reciprocal square root and reciprocal, each within a few ulp), which keeps
 // the update well inside the float32 tolerance at a fraction of the
 // instructions of the correctly rounded sequences.
-__device__ __forceinline__ void adagrad_elem(float& w, float& a, float g, float lr, float eps) {
-  a = fmaf(g, g, a);
-  const float sq = a > 0.f ? a * rsqrtf(a) : 0.f;
-  w -= __fdividef(lr * g, sq + eps);
+struct AdagradStep {
+  static constexpr bool kZ = false;  // no second state array
+  float lr, eps;
+  __device__ __forceinline__ void elem(float& w, float& a, float& /*z*/, float g) const {
+    a = fmaf(g, g, a);
+    const float sq = a > 0.f ? a * rsqrtf(a) : 0.f;
+    w -= __fdividef(lr * g, sq + eps);
+  }
+};
+
+// FTRL-Proximal, the other sparse optimizer the JD ads article names (3.2.1),
+// in the per-coordinate form of McMahan et al., "Ad Click Prediction: a View
+// from the Trenches" (KDD 2013), Algorithm 1; the accumulator array holds n
+// and a second array holds z:
+//   sigma = (sqrt(n + g*g) - sqrt(n)) / alpha;  z += g - sigma * w;  n += g*g;
+//   w = 0 if |z| <= lambda1, else -(z - sign(z) lambda1) / ((beta + sqrt(n)) / alpha + lambda2)
+// with w on the right of the z update the weight the forward used.  Correctly
+// rounded float32 operations in this order, none contracted: the difference
+// of square roots cancels when g*g << n, and the same rounding sequence as
+// the oracle's keeps that cancellation identical on both sides.
+struct FtrlStep {
+  static constexpr bool kZ = true;
+  float alpha, beta, l1, l2;
+  __device__ __forceinline__ void elem(float& w, float& n, float& z, float g) const {
+    const float n1 = __fadd_rn(n, __fmul_rn(g, g));
+    const float sn = __fsqrt_rn(n), sn1 = __fsqrt_rn(n1);
+    const float sigma = __fdiv_rn(__fsub_rn(sn1, sn), alpha);
+    z = __fsub_rn(__fadd_rn(z, g), __fmul_rn(sigma, w));
+    n = n1;
+    if (fabsf(z) <= l1) {
+      w = 0.f;
+    } else {
+      const float num = __fsub_rn(z, z > 0.f ? l1 : -l1);
+      const float den = __fadd_rn(__fdiv_rn(__fadd_rn(beta, sn1), alpha), l2);
+      w = -__fdiv_rn(num, den);
+    }
+  }
+};
+
+// The update of 4 consecutive elements from e: weights, accumulators (and z)
+// read, updated and written back with evict-first stores; for master-copy
+// tables (W the f32 masters) the f16 copy the forward reads is written from
+// the new masters too, rounded to nearest-even.
+template <typename TW, typename Opt>
+__device__ __forceinline__ void update4(const TableView& t, long long e, const float* g, const Opt& o) {
+  TW* W = static_cast<TW*>(t.W);
+  const float4 a = *reinterpret_cast<const float4*>(t.ACC + e);
+  float av[4] = {a.x, a.y, a.z, a.w};
+  float zv[4] = {0.f, 0.f, 0.f, 0.f};
+  if (Opt::kZ) {
+    const float4 z = *reinterpret_cast<const float4*>(t.Z + e);
+    zv[0] = z.x; zv[1] = z.y; zv[2] = z.z; zv[3] = z.w;
+  }
+  float wv[4];
+  ldw4(W + e, wv);
+#pragma unroll
+  for (int j = 0; j < 4; ++j) o.elem(wv[j], av[j], zv[j], g[j]);
+  __stcs(reinterpret_cast<float4*>(t.ACC + e), make_float4(av[0], av[1], av[2], av[3]));
+  if (Opt::kZ) __stcs(reinterpret_cast<float4*>(t.Z + e), make_float4(zv[0], zv[1], zv[2], zv[3]));
+  stw4(W + e, wv);
+  if (std::is_same<TW, float>::value && t.W16) stw4(t.W16 + e, wv);
 }
 
-// Element-wise Adagrad on one lane's columns of one row.
-template <typename TW, int NCB>
-__device__ __forceinline__ void adagrad_row(const TableView& t, long long e0, int D, int G, int li,
-                                            const float (&g)[NCB][4], float lr, float eps) {
-  TW* W = static_cast<TW*>(t.W);
+// The update on one lane's columns of one row (the fixup).
+template <typename TW, int NCB, typename Opt>
+__device__ __forceinline__ void update_row(const TableView& t, long long e0, int D, int G, int li,
+                                           const float (&g)[NCB][4], const Opt& o) {
 #pragma unroll
   for (int c = 0; c < NCB; ++c) {
     const int ce = (c * G + li) * 4;
-    if (ce < D) {
-      const float4 a = *reinterpret_cast<const float4*>(t.ACC + e0 + ce);
-      float av[4] = {a.x, a.y, a.z, a.w};
-      float wv[4];
-      ldw4(W + e0 + ce, wv);
-#pragma unroll
-      for (int j = 0; j < 4; ++j) adagrad_elem(wv[j], av[j], g[c][j], lr, eps);
-      *reinterpret_cast<float4*>(t.ACC + e0 + ce) = make_float4(av[0], av[1], av[2], av[3]);
-      stw4(W + e0 + ce, wv);
-    }
+    if (ce < D) update4<TW>(t, e0 + ce, g[c], o);
   }
 }
 
@@ -535,22 +739,11 @@ __device__ __forceinline__ void row_geom(const TableView& t, unsigned row, int& 
   }
 }
 
-// Element-wise Adagrad on VW consecutive columns starting at element e (VW a
-// multiple of 4).
-template <typename TW, int VW>
-__device__ __forceinline__ void adagrad_cols(const TableView& t, long long e, const float* g, float lr, float eps) {
-  TW* W = static_cast<TW*>(t.W);
+// The update on VW consecutive columns starting at element e (VW a multiple of 4).
+template <typename TW, int VW, typename Opt>
+__device__ __forceinline__ void update_cols(const TableView& t, long long e, const float* g, const Opt& o) {
 #pragma unroll
-  for (int h = 0; h < VW; h += 4) {
-    const float4 a = *reinterpret_cast<const float4*>(t.ACC + e + h);
-    float av[4] = {a.x, a.y, a.z, a.w};
-    float wv[4];
-    ldw4(W + e + h, wv);
-#pragma unroll
-    for (int j = 0; j < 4; ++j) adagrad_elem(wv[j], av[j], g[h + j], lr, eps);
-    __stcs(reinterpret_cast<float4*>(t.ACC + e + h), make_float4(av[0], av[1], av[2], av[3]));
-    stw4(W + e + h, wv);
-  }
+  for (int h = 0; h < VW; h += 4) update4<TW>(t, e + h, g + h, o);
 }
 
 // Geometry of a row taken from the feature slot of a bag that holds it (the
@@ -691,12 +884,12 @@ __device__ __forceinline__ void fma_vw(float* acc, float w, const float* g) {
 }
 
 // kAllCols: every lane column is inside every row (one dim, equal to G x VW x NCB).
-template <typename TW, int G, int VW, int NCB, int U, bool kAllCols>
-__global__ void __launch_bounds__(kRedWarps * 32, 10) segreduce_adagrad_kernel(
+template <typename TW, int G, int VW, int NCB, int U, bool kAllCols, typename Opt>
+__global__ void __launch_bounds__(kRedWarps * 32, 10) segreduce_update_kernel(
     TableView t, const unsigned* __restrict__ K, const unsigned* __restrict__ V, const float* __restrict__ scale,
     int mean, const float* __restrict__ grad, const float* __restrict__ zrow, unsigned n, unsigned n_bags,
-    unsigned n_chunks, float* __restrict__ partA, float* __restrict__ partB, unsigned* __restrict__ arow, float lr,
-    float eps, unsigned* __restrict__ work) {
+    unsigned n_chunks, float* __restrict__ partA, float* __restrict__ partB, unsigned* __restrict__ arow, Opt opt,
+    unsigned* __restrict__ work) {
   constexpr int P = 32 / G;
   constexpr int CW = G * VW * NCB;      // columns a group covers
   constexpr int UW = U < G ? U : G;     // positions per walk step (a window holds G)
@@ -763,7 +956,7 @@ __global__ void __launch_bounds__(kRedWarps * 32, 10) segreduce_adagrad_kernel(
 #pragma unroll
           for (int cc = 0; cc < NCB; ++cc) {
             const int col = (cc * G + li) * VW;
-            if (col < sm.D) adagrad_cols<TW, VW>(t, sm.e0 + col, &st[f][col], lr, eps);
+            if (col < sm.D) update_cols<TW, VW>(t, sm.e0 + col, &st[f][col], opt);
           }
         } else {
           float* dst = ((sm.flags & 1) ? partA : partB) + (size_t)c * maxd;
@@ -892,11 +1085,11 @@ __global__ void __launch_bounds__(kRedWarps * 32, 10) segreduce_adagrad_kernel(
 
 // ------------------------------------------------------------------ 4. fixup of spanning segments
 
-template <typename TW, int G, int NCB>
+template <typename TW, int G, int NCB, typename Opt>
 __global__ void __launch_bounds__(256) fixup_kernel(TableView t, const unsigned* __restrict__ K, unsigned n,
                                                     unsigned n_chunks, const float* __restrict__ partA,
                                                     const float* __restrict__ partB,
-                                                    const unsigned* __restrict__ arow, float lr, float eps) {
+                                                    const unsigned* __restrict__ arow, Opt opt) {
   constexpr int P = 32 / G;
   const int lane = threadIdx.x & 31;
   const int sub = lane / G, li = lane % G;
@@ -971,46 +1164,7 @@ __global__ void __launch_bounds__(256) fixup_kernel(TableView t, const unsigned*
         }
         acc[cc][j] = __fadd_rn(acc[cc][j], cmp[cc][j]);
       }
-    if (sub == 0) adagrad_row<TW, NCB>(t, e0, D, G, li, acc, lr, eps);
-  }
-}
-
-// ------------------------------------------------------------------ 5. f16 copy of master-copy tables
-//
-// Mixed precision as the JD article describes it (3.2.3): the update works on
-// the f32 master rows (the f32 reduce above, with W the master); the forward
-// reads their f16 copy, refreshed here for every row the step updated (the
-// run heads of the sorted pairs), rounded to nearest-even.  One warp per 32
-// sorted positions copies each row that starts among them, four elements
-// per lane.
-__global__ void __launch_bounds__(256) refresh_half_kernel(TableView t, const unsigned* __restrict__ K, unsigned n,
-                                                           __half* __restrict__ W16) {
-  const int lane = threadIdx.x & 31;
-  const unsigned nw = (gridDim.x * blockDim.x) >> 5;
-  const unsigned miss = t.n_rows;
-  const float* M = static_cast<const float*>(t.W);
-  for (unsigned w = (blockIdx.x * blockDim.x + threadIdx.x) >> 5; (size_t)w * 32 < n; w += nw) {
-    const unsigned i = w * 32 + lane;
-    const unsigned k = i < n ? K[i] : miss;
-    const unsigned kp = (i < n && i > 0) ? K[i - 1] : kNoRow;
-    unsigned heads = __ballot_sync(0xffffffffu, i < n && k < miss && k != kp);
-    while (heads) {
-      const int j = __ffs(heads) - 1;
-      heads &= heads - 1;
-      const unsigned row = __shfl_sync(0xffffffffu, k, j);
-      int D, col;
-      long long e0;
-      row_geom(t, row, D, col, e0);
-      for (int c = lane * 4; c < D; c += 128) {  // D is a multiple of 8 for tables with f16 rows
-        const float4 m = *reinterpret_cast<const float4*>(M + e0 + c);
-        const __half2 a = __floats2half2_rn(m.x, m.y);
-        const __half2 b = __floats2half2_rn(m.z, m.w);
-        uint2 x;
-        x.x = *reinterpret_cast<const unsigned*>(&a);
-        x.y = *reinterpret_cast<const unsigned*>(&b);
-        *reinterpret_cast<uint2*>(W16 + e0 + c) = x;
-      }
-    }
+    if (sub == 0) update_row<TW, NCB>(t, e0, D, G, li, acc, opt);
   }
 }
 
@@ -1074,18 +1228,18 @@ static void mark_phase(const emb_table* t, int phase, cudaStream_t st) {
     cudaEventRecord((cudaEvent_t)t->phase_events[phase], st);
 }
 
-template <typename TW, int G, int VW, int NCB>
+template <typename TW, int G, int VW, int NCB, typename Opt>
 static cudaError_t launch_reduce(const emb_table* t, const unsigned* K, const unsigned* V, const float* scale,
                                  int mean, const float* grad, unsigned n, unsigned n_bags, const WsLayout& L, char* ws,
-                                 float lr, float eps, cudaStream_t st) {
+                                 const Opt& opt, cudaStream_t st) {
   constexpr int U = NCB >= 4 ? 1 : 4 / NCB;  // grad_out vectors in flight per lane (measured best at 4)
   constexpr int P = 32 / G;
   TableView v = t->view();
   const int threads = kRedWarps * 32;
   int per_sm = 0;
   const bool all_cols = t->uniform_dim == G * VW * NCB;
-  auto kern = all_cols ? segreduce_adagrad_kernel<TW, G, VW, NCB, U, true>
-                       : segreduce_adagrad_kernel<TW, G, VW, NCB, U, false>;
+  auto kern = all_cols ? segreduce_update_kernel<TW, G, VW, NCB, U, true, Opt>
+                       : segreduce_update_kernel<TW, G, VW, NCB, U, false, Opt>;
   cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, threads, 0);
   long long blocks = ((long long)L.n_chunks + (threads / 32) * P - 1) / ((threads / 32) * P);
   blocks = std::min<long long>(blocks, (long long)std::max(1, per_sm) * sm_count());
@@ -1103,14 +1257,14 @@ static cudaError_t launch_reduce(const emb_table* t, const unsigned* K, const un
   e = cudaMemsetAsync(work, 0, sizeof(unsigned), st);
   if (e != cudaSuccess) return e;
   kern<<<(int)std::max(1LL, blocks), threads, 0, st>>>(
-      v, K, V, scale, mean, grad, zrow, n, n_bags, L.n_chunks, pa, pb, ar, lr, eps, work);
+      v, K, V, scale, mean, grad, zrow, n, n_bags, L.n_chunks, pa, pb, ar, opt, work);
   mark_phase(t, 2, st);
   // the fixup reads partial rows four columns per lane
   constexpr int G4 = G * VW / 4 > 32 ? 32 : G * VW / 4;
   constexpr int NCB4 = (G * VW * NCB) / (4 * G4);
   long long fblocks = std::min<long long>(((long long)L.n_chunks * 32 + 255) / 256, resident_blocks(256));
-  fixup_kernel<TW, G4, NCB4><<<(int)std::max(1LL, fblocks), 256, 0, st>>>(v, K, n, L.n_chunks, pa, pb, ar, lr,
-                                                                              eps);
+  fixup_kernel<TW, G4, NCB4, Opt><<<(int)std::max(1LL, fblocks), 256, 0, st>>>(v, K, n, L.n_chunks, pa, pb, ar,
+                                                                                   opt);
   mark_phase(t, 3, st);
   return cudaGetLastError();
 }
@@ -1119,12 +1273,12 @@ static cudaError_t launch_reduce(const emb_table* t, const unsigned* K, const un
 // wider rows give each lane several column blocks.  (32-byte vectors with
 // half the lanes per row measured slower at 100M keys x dim 128: they cost
 // registers, and resident warps matter more here than load width.)
-template <typename TW>
+template <typename TW, typename Opt>
 static cudaError_t dispatch_reduce(const emb_table* t, const unsigned* K, const unsigned* V, const float* scale,
                                    int mean, const float* grad, unsigned n, unsigned n_bags, const WsLayout& L,
-                                   char* ws, float lr, float eps, cudaStream_t st) {
+                                   char* ws, const Opt& opt, cudaStream_t st) {
   const int md = t->st.max_dim;
-#define EMB_RED(G, VW, NCB) return launch_reduce<TW, G, VW, NCB>(t, K, V, scale, mean, grad, n, n_bags, L, ws, lr, eps, st)
+#define EMB_RED(G, VW, NCB) return launch_reduce<TW, G, VW, NCB>(t, K, V, scale, mean, grad, n, n_bags, L, ws, opt, st)
   if (md <= 4) EMB_RED(1, 4, 1);
   if (md <= 8) EMB_RED(2, 4, 1);
   if (md <= 16) EMB_RED(4, 4, 1);
@@ -1142,24 +1296,55 @@ static int bits_for(unsigned x) {
   return b;
 }
 
+// Radix passes: in-slot row numbers and the miss code (the slot's row count)
+// of the largest slot fit in `bits`.
 static int sort_passes(const emb_table* t) {
-  const int bits = bits_for((unsigned)t->st.n_keys);  // rows and the miss sentinel fit in `bits`
+  const int bits = bits_for((unsigned)t->st.max_slot_keys);
   return std::max(1, (bits + kRadixBits - 1) / kRadixBits);
 }
+
+// Slot-major placement of the pairs: dest (three scan launches over the bag
+// lengths) and the workspace header + sort regions (one launch).
+static emb_status launch_placement(const emb_table* t, const int64_t* offsets_d, long long n_bags, long long nnz,
+                                   char* ws, const WsLayout& L, cudaStream_t st) {
+  WsHeader* hdr = (WsHeader*)(ws + L.hdr);
+  unsigned* dest = (unsigned*)(ws + L.dest);
+  unsigned* partials = (unsigned*)(ws + L.partials);
+  const unsigned S = (unsigned)t->st.n_slots;
+  const unsigned long long B = (unsigned long long)n_bags / S;
+  EMB_CUDA(cudaMemsetAsync(&hdr->total, 0, sizeof(unsigned long long), st));
+  if (n_bags > 0) {
+    const unsigned np = (unsigned)((n_bags + kScanTile - 1) / kScanTile);
+    len_scan_reduce_kernel<<<np, kScanThreads, 0, st>>>((const long long*)offsets_d, B, S, nnz, (size_t)n_bags,
+                                                         partials, hdr);
+    scan_partials_kernel<<<1, 1024, 0, st>>>(partials, np);
+    len_scan_down_kernel<<<np, kScanThreads, 0, st>>>((const long long*)offsets_d, B, S, nnz, (size_t)n_bags, dest,
+                                                       partials);
+  }
+  seg_setup_kernel<<<1, 1024, 0, st>>>(t->view(), hdr, (unsigned)nnz, (unsigned long long)n_bags,
+                                       (unsigned)(sort_passes(t) & 1), dest, (SortSeg*)(ws + L.sseg));
+  EMB_CUDA(cudaGetLastError());
+  return EMB_OK;
+}
+
+// The optimizer of one backward call.
+struct BwdOpt {
+  bool ftrl;
+  AdagradStep ada;
+  FtrlStep fp;
+};
 
 // The backward.  With `recorded`, the (row, bag) pairs, 1/L and the header were
 // written by emb_lookup_fwd_record and the expand phase is skipped.
 static emb_status run_bwd(emb_table* table, const int64_t* offsets_d, int64_t n_bags, const int64_t* keys_d,
-                          int64_t nnz, emb_pool pool, const float* grad_out_d, float lr, float eps, char* ws,
+                          int64_t nnz, emb_pool pool, const float* grad_out_d, const BwdOpt& opt, char* ws,
                           const WsLayout& L, cudaStream_t st, bool recorded = false) {
   const unsigned n = (unsigned)nnz;
   // grad_out rows are addressed as 32-bit float4 indices
   if ((unsigned long long)(n_bags / table->st.n_slots) * (unsigned long long)table->st.sum_dims >= (1ULL << 34))
     return fail(EMB_ERR_UNSUPPORTED, "grad_out larger than 2^34 elements");
   const int passes = sort_passes(table);
-  const unsigned sorted_in_b = (unsigned)(passes & 1);
   TableView v = table->view();
-  WsHeader* hdr = (WsHeader*)(ws + L.hdr);
   unsigned* kA = (unsigned*)(ws + L.kA);
   unsigned* kB = (unsigned*)(ws + L.kB);
   unsigned* vA = (unsigned*)(ws + L.vA);
@@ -1167,14 +1352,15 @@ static emb_status run_bwd(emb_table* table, const int64_t* offsets_d, int64_t n_
   float* scale = (float*)(ws + L.scale);
   const int mean = pool == EMB_POOL_MEAN;
 
-  // With malformed offsets (flagged) the expand step (or the recording
-  // forward) writes positions outside every bag as absent pairs; every later
-  // kernel treats rows >= n_rows and bags >= n_bags as absent.
+  // Every later kernel treats rows >= n_rows and bags >= n_bags as absent
+  // (misses, and with malformed offsets every position: see seg_setup_kernel).
   if (!recorded) {
+    emb_status rc = launch_placement(table, offsets_d, n_bags, nnz, ws, L, st);
+    if (rc != EMB_OK) return rc;
     long long blocks = std::min<long long>((n_bags * 32 + 255) / 256, resident_blocks(256));
     expand_kernel<<<(int)std::max(1LL, blocks), 256, 0, st>>>(v, (const long long*)offsets_d, n_bags,
-                                                              (const long long*)keys_d, nnz, mean, kA, vA, scale,
-                                                              hdr, sorted_in_b);
+                                                              (const long long*)keys_d, nnz, mean,
+                                                              (const unsigned*)(ws + L.dest), kA, vA, scale);
     EMB_CUDA(cudaGetLastError());
   }
   mark_phase(table, 0, st);
@@ -1188,28 +1374,29 @@ static emb_status run_bwd(emb_table* table, const int64_t* offsets_d, int64_t n_
   const size_t smem = scatter_smem();
   EMB_CUDA(cudaFuncSetAttribute(radix_scatter_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem));
   unsigned *ki = kA, *vi = vA, *ko = kB, *vo = vB;
+  const SortSeg* sg = (const SortSeg*)(ws + L.sseg);
   for (int p = 0; p < passes; ++p) {
     const int shift = p * kRadixBits;
-    radix_count_kernel<<<L.n_tiles_sort, kSortThreads, 0, st>>>(ki, n, shift, counts, L.n_tiles_sort);
+    radix_count_kernel<<<L.n_tiles_sort, kSortThreads, 0, st>>>(ki, sg, L.n_regions, shift, counts);
     EMB_CUDA(launch_scan(counts, counts, (size_t)kDigits * L.n_tiles_sort, partials, st));
-    radix_scatter_kernel<<<L.n_tiles_sort, kSortThreads, smem, st>>>(ki, vi, ko, vo, n, shift, counts,
-                                                                     L.n_tiles_sort);
+    radix_scatter_kernel<<<L.n_tiles_sort, kSortThreads, smem, st>>>(ki, vi, ko, vo, shift, counts, sg, L.n_regions,
+                                                                     (unsigned)table->st.n_keys, (unsigned)n_bags);
     EMB_CUDA(cudaGetLastError());
     std::swap(ki, ko);
     std::swap(vi, vo);
   }
   mark_phase(table, 1, st);
   // ki/vi hold the sorted pairs
-  cudaError_t e = table->st.wdtype == EMB_F16
-                      ? dispatch_reduce<__half>(table, ki, vi, scale, mean, grad_out_d, n, (unsigned)n_bags, L, ws, lr, eps, st)
-                      : dispatch_reduce<float>(table, ki, vi, scale, mean, grad_out_d, n, (unsigned)n_bags, L, ws, lr, eps, st);
+  const bool half = table->st.wdtype == EMB_F16;
+  const unsigned nb = (unsigned)n_bags;
+  cudaError_t e;
+  if (opt.ftrl)
+    e = half ? dispatch_reduce<__half>(table, ki, vi, scale, mean, grad_out_d, n, nb, L, ws, opt.fp, st)
+             : dispatch_reduce<float>(table, ki, vi, scale, mean, grad_out_d, n, nb, L, ws, opt.fp, st);
+  else
+    e = half ? dispatch_reduce<__half>(table, ki, vi, scale, mean, grad_out_d, n, nb, L, ws, opt.ada, st)
+             : dispatch_reduce<float>(table, ki, vi, scale, mean, grad_out_d, n, nb, L, ws, opt.ada, st);
   if (e != cudaSuccess) return cuda_fail(e, "segmented reduce launch");
-  if (table->W16_d && n > 0) {  // master-copy table: the forward's f16 rows follow the updated masters
-    const long long blocks = std::min<long long>(((long long)n + 255) / 256, resident_blocks(256));
-    refresh_half_kernel<<<(int)std::max(1LL, blocks), 256, 0, st>>>(v, ki, n, (__half*)table->W16_d);
-    e = cudaGetLastError();
-    if (e != cudaSuccess) return cuda_fail(e, "f16 copy refresh launch");
-  }
   return EMB_OK;
 }
 
@@ -1285,6 +1472,7 @@ emb_status emb_bwd_adagrad_noalloc(emb_table* table, const int64_t* offsets_d, i
                                    void* stream) {
   emb_status rc = check_batch(table, offsets_d, n_bags, keys_d, nnz, pool);
   if (rc != EMB_OK) return rc;
+  if (table->optimizer != EMB_OPT_ADAGRAD) return fail(EMB_ERR_INVALID_ARG, "the table's optimizer is not Adagrad");
   if (n_bags > 0 && !grad_out_d) return fail(EMB_ERR_INVALID_ARG, "grad_out is NULL");
   if (((uintptr_t)grad_out_d & 15) != 0) return fail(EMB_ERR_INVALID_ARG, "grad_out must be 16-byte aligned");
   const WsLayout L = ws_layout(table, n_bags, nnz);
@@ -1297,8 +1485,8 @@ emb_status emb_bwd_adagrad_noalloc(emb_table* table, const int64_t* offsets_d, i
   }
   void* scratch = nullptr;
   if ((rc = noalloc_scratch(&scratch)) != EMB_OK) return rc;
-  return run_bwd(table, offsets_d, n_bags, keys_d, nnz, pool, grad_out_d, lr, eps, (char*)scratch, L,
-                 (cudaStream_t)stream);
+  return run_bwd(table, offsets_d, n_bags, keys_d, nnz, pool, grad_out_d, BwdOpt{false, {lr, eps}, {}},
+                 (char*)scratch, L, (cudaStream_t)stream);
 }
 
 emb_status emb_lookup_fwd_record(emb_table* table, const int64_t* offsets_d, int64_t n_bags, const int64_t* keys_d,
@@ -1313,9 +1501,7 @@ emb_status emb_lookup_fwd_record(emb_table* table, const int64_t* offsets_d, int
   if (((uintptr_t)workspace_d & 255) != 0) return fail(EMB_ERR_WORKSPACE, "workspace must be 256-byte aligned");
   cudaStream_t st = (cudaStream_t)stream;
   char* ws = (char*)workspace_d;
-  ws_header_kernel<<<1, 256, 0, st>>>((WsHeader*)(ws + L.hdr), (unsigned)nnz, (unsigned)n_bags,
-                                      (unsigned)(sort_passes(table) & 1), (unsigned)table->st.n_keys,
-                                      (const long long*)offsets_d, (unsigned*)(ws + L.kA), (unsigned*)(ws + L.vA));
+  if ((rc = launch_placement(table, offsets_d, n_bags, nnz, ws, L, st)) != EMB_OK) return rc;
   if (n_bags > 0) {
     // bags are handed out in order from a counter (measured 17.7 -> 15.1 ms at
     // 100M keys x dim 128 against a static order; Zipf bag lengths unbalance it)
@@ -1323,7 +1509,7 @@ emb_status emb_lookup_fwd_record(emb_table* table, const int64_t* offsets_d, int
     EMB_CUDA(cudaMemsetAsync(fwork, 0, sizeof(unsigned long long), st));
     cudaError_t e = launch_forward(table, (const long long*)offsets_d, n_bags, (const long long*)keys_d, nnz,
                                    pool == EMB_POOL_MEAN, out_d, (unsigned*)(ws + L.kA), (unsigned*)(ws + L.vA),
-                                   (float*)(ws + L.scale), fwork, st);
+                                   (float*)(ws + L.scale), (const unsigned*)(ws + L.dest), fwork, st);
     if (e != cudaSuccess) return cuda_fail(e, "fwd_pool_kernel launch");
   }
   EMB_CUDA(cudaGetLastError());
@@ -1334,10 +1520,12 @@ emb_status emb_lookup_fwd_record(emb_table* table, const int64_t* offsets_d, int
   return EMB_OK;
 }
 
-emb_status emb_bwd_adagrad_recorded(emb_table* table, int64_t n_bags, int64_t nnz, emb_pool pool,
-                                    const float* grad_out_d, float lr, float eps, void* workspace_d, size_t ws_bytes,
-                                    void* stream) {
+// The recorded backward with either optimizer.
+static emb_status bwd_recorded(emb_table* table, int64_t n_bags, int64_t nnz, emb_pool pool, const float* grad_out_d,
+                               const BwdOpt& opt, void* workspace_d, size_t ws_bytes, void* stream) {
   if (!table) return fail(EMB_ERR_INVALID_ARG, "table is NULL");
+  if (table->optimizer != (opt.ftrl ? EMB_OPT_FTRL : EMB_OPT_ADAGRAD))
+    return fail(EMB_ERR_INVALID_ARG, "the table was created for the other optimizer");
   if (!workspace_d || workspace_d != table->rec_ws || nnz != table->rec_nnz || n_bags != table->rec_bags ||
       (int)pool != table->rec_pool)
     return fail(EMB_ERR_INVALID_ARG, "no emb_lookup_fwd_record of this batch shape in this workspace");
@@ -1345,8 +1533,58 @@ emb_status emb_bwd_adagrad_recorded(emb_table* table, int64_t n_bags, int64_t nn
   if (((uintptr_t)grad_out_d & 15) != 0) return fail(EMB_ERR_INVALID_ARG, "grad_out must be 16-byte aligned");
   const WsLayout L = ws_layout(table, n_bags, nnz);
   if (ws_bytes < L.total) return fail(EMB_ERR_WORKSPACE, "workspace missing or too small");
-  return run_bwd(table, nullptr, n_bags, nullptr, nnz, pool, grad_out_d, lr, eps, (char*)workspace_d, L,
+  return run_bwd(table, nullptr, n_bags, nullptr, nnz, pool, grad_out_d, opt, (char*)workspace_d, L,
                  (cudaStream_t)stream, true);
+}
+
+// The backward with a caller workspace and either optimizer.
+static emb_status bwd_workspace(emb_table* table, const int64_t* offsets_d, int64_t n_bags, const int64_t* keys_d,
+                                int64_t nnz, emb_pool pool, const float* grad_out_d, const BwdOpt& opt,
+                                void* workspace_d, size_t ws_bytes, void* stream) {
+  emb_status rc = check_batch(table, offsets_d, n_bags, keys_d, nnz, pool);
+  if (rc != EMB_OK) return rc;
+  if (table->optimizer != (opt.ftrl ? EMB_OPT_FTRL : EMB_OPT_ADAGRAD))
+    return fail(EMB_ERR_INVALID_ARG, "the table was created for the other optimizer");
+  if (n_bags > 0 && !grad_out_d) return fail(EMB_ERR_INVALID_ARG, "grad_out is NULL");
+  if (((uintptr_t)grad_out_d & 15) != 0) return fail(EMB_ERR_INVALID_ARG, "grad_out must be 16-byte aligned");
+  const WsLayout L = ws_layout(table, n_bags, nnz);
+  if (!workspace_d || ws_bytes < L.total) return fail(EMB_ERR_WORKSPACE, "workspace missing or too small");
+  if (((uintptr_t)workspace_d & 255) != 0) return fail(EMB_ERR_WORKSPACE, "workspace must be 256-byte aligned");
+  return run_bwd(table, offsets_d, n_bags, keys_d, nnz, pool, grad_out_d, opt, (char*)workspace_d, L,
+                 (cudaStream_t)stream);
+}
+
+static emb_status ftrl_opt(const emb_ftrl_params* p, BwdOpt* o) {
+  if (!p) return fail(EMB_ERR_INVALID_ARG, "FTRL parameters are NULL");
+  if (!(p->alpha > 0.f) || !(p->beta >= 0.f) || !(p->lambda1 >= 0.f) || !(p->lambda2 >= 0.f))
+    return fail(EMB_ERR_INVALID_ARG, "FTRL needs alpha > 0 and beta, lambda1, lambda2 >= 0");
+  *o = BwdOpt{true, {}, {p->alpha, p->beta, p->lambda1, p->lambda2}};
+  return EMB_OK;
+}
+
+emb_status emb_bwd_adagrad_recorded(emb_table* table, int64_t n_bags, int64_t nnz, emb_pool pool,
+                                    const float* grad_out_d, float lr, float eps, void* workspace_d, size_t ws_bytes,
+                                    void* stream) {
+  return bwd_recorded(table, n_bags, nnz, pool, grad_out_d, BwdOpt{false, {lr, eps}, {}}, workspace_d, ws_bytes,
+                      stream);
+}
+
+emb_status emb_bwd_ftrl_recorded(emb_table* table, int64_t n_bags, int64_t nnz, emb_pool pool,
+                                 const float* grad_out_d, const emb_ftrl_params* params, void* workspace_d,
+                                 size_t ws_bytes, void* stream) {
+  BwdOpt o;
+  emb_status rc = ftrl_opt(params, &o);
+  if (rc != EMB_OK) return rc;
+  return bwd_recorded(table, n_bags, nnz, pool, grad_out_d, o, workspace_d, ws_bytes, stream);
+}
+
+emb_status emb_bwd_ftrl(emb_table* table, const int64_t* offsets_d, int64_t n_bags, const int64_t* keys_d,
+                        int64_t nnz, emb_pool pool, const float* grad_out_d, const emb_ftrl_params* params,
+                        void* workspace_d, size_t ws_bytes, void* stream) {
+  BwdOpt o;
+  emb_status rc = ftrl_opt(params, &o);
+  if (rc != EMB_OK) return rc;
+  return bwd_workspace(table, offsets_d, n_bags, keys_d, nnz, pool, grad_out_d, o, workspace_d, ws_bytes, stream);
 }
 
 emb_status emb_bwd_phase_events(emb_table* table, void* const* events, int n) {
@@ -1367,15 +1605,8 @@ emb_status emb_bwd_workspace_size(const emb_table* table, int64_t n_bags, int64_
 emb_status emb_bwd_adagrad(emb_table* table, const int64_t* offsets_d, int64_t n_bags, const int64_t* keys_d,
                            int64_t nnz, emb_pool pool, const float* grad_out_d, float lr, float eps,
                            void* workspace_d, size_t ws_bytes, void* stream) {
-  emb_status rc = check_batch(table, offsets_d, n_bags, keys_d, nnz, pool);
-  if (rc != EMB_OK) return rc;
-  if (n_bags > 0 && !grad_out_d) return fail(EMB_ERR_INVALID_ARG, "grad_out is NULL");
-  if (((uintptr_t)grad_out_d & 15) != 0) return fail(EMB_ERR_INVALID_ARG, "grad_out must be 16-byte aligned");
-  const WsLayout L = ws_layout(table, n_bags, nnz);
-  if (!workspace_d || ws_bytes < L.total) return fail(EMB_ERR_WORKSPACE, "workspace missing or too small");
-  if (((uintptr_t)workspace_d & 255) != 0) return fail(EMB_ERR_WORKSPACE, "workspace must be 256-byte aligned");
-  return run_bwd(table, offsets_d, n_bags, keys_d, nnz, pool, grad_out_d, lr, eps, (char*)workspace_d, L,
-                 (cudaStream_t)stream);
+  return bwd_workspace(table, offsets_d, n_bags, keys_d, nnz, pool, grad_out_d, BwdOpt{false, {lr, eps}, {}},
+                       workspace_d, ws_bytes, stream);
 }
 
 emb_status emb_bwd_unique_keys(const emb_table* table, const void* workspace_d, size_t ws_bytes, int64_t* keys_out_d,

@@ -73,11 +73,13 @@ __device__ __forceinline__ int pow2_at_least(int x) {
 
 // With a Record sink the kernel also writes, for the backward, the resolved
 // internal row of every occurrence (n_rows for a miss) and its bag, plus 1/L
-// per bag for mean pooling.
+// per bag for mean pooling.  The pairs go to the bag's place in slot-major
+// order (dest), so the backward's sort only has to order rows within a slot.
 struct Record {
   unsigned* K;
   unsigned* V;
   float* scale;
+  const unsigned* dest;      // per bag: first position of its pairs in slot-major order
   unsigned long long* work;  // optional bag counter: bags taken in batches, in order
 };
 
@@ -140,6 +142,8 @@ __global__ void __launch_bounds__(256, 8) fwd_pool_kernel(TableView t, const lon
       start = min(max(start, 0LL), nnz);
       end = min(max(end, start), nnz);
     }
+    // where this bag's pairs go (inside [0, nnz) unless the offsets are malformed)
+    const long long d0 = kRecord ? (long long)rec.dest[bag] - start : 0;
     float acc[NCB][VEC];
 #pragma unroll
     for (int c = 0; c < NCB; ++c)
@@ -163,8 +167,11 @@ __global__ void __launch_bounds__(256, 8) fwd_pool_kernel(TableView t, const lon
           }
         }
         if (kRecord) {
-          rec.K[c0 + tl] = row;
-          rec.V[c0 + tl] = (unsigned)bag;
+          const long long p = d0 + c0 + tl;
+          if (p < nnz) {
+            rec.K[p] = row;
+            rec.V[p] = (unsigned)bag;
+          }
         }
       }
       for (int base = 0; base < n; base += P * U) {
@@ -264,8 +271,8 @@ static cudaError_t launch_fwd(const emb_table* t, const long long* offsets, long
 // Forward launch, optionally recording (row, bag) pairs for the backward.
 cudaError_t launch_forward(const emb_table* t, const long long* offsets, long long n_bags, const long long* keys,
                            long long nnz, int mean, float* out, unsigned* K, unsigned* V, float* scale,
-                           unsigned long long* work, cudaStream_t st) {
-  const Record rec{K, V, scale, work};
+                           const unsigned* dest, unsigned long long* work, cudaStream_t st) {
+  const Record rec{K, V, scale, dest, work};
   const bool record = K != nullptr;
   if (t->fwd_half())
     return record ? launch_fwd<__half, true>(t, offsets, n_bags, keys, nnz, mean, out, rec, st)
@@ -299,7 +306,7 @@ extern "C" emb_status emb_lookup_fwd(emb_table* table, const int64_t* offsets_d,
   if (((uintptr_t)out_d & 15) != 0) return fail(EMB_ERR_INVALID_ARG, "out must be 16-byte aligned");
   cudaStream_t st = (cudaStream_t)stream;
   cudaError_t e = launch_forward(table, (const long long*)offsets_d, n_bags, (const long long*)keys_d, nnz,
-                                 pool == EMB_POOL_MEAN, out_d, nullptr, nullptr, nullptr, nullptr, st);
+                                 pool == EMB_POOL_MEAN, out_d, nullptr, nullptr, nullptr, nullptr, nullptr, st);
   if (e != cudaSuccess) return cuda_fail(e, "fwd_pool_kernel launch");
   return EMB_OK;
 }

@@ -11,6 +11,7 @@
 //   ACC     f32[n_elems]     Adagrad accumulators, same layout as W.
 //   W16     f16[n_elems]     EMB_F16_MASTER tables only: the f16 copy of W
 //                            (then the f32 master) that the forward reads.
+//   Z       f32[n_elems]     EMB_OPT_FTRL tables only: FTRL's z (ACC is n).
 //   row_key int64[n_rows]    key of each internal row.
 //   int_to_ext / ext_to_int  u32[n_rows] row-order permutations.
 //   flags   u32              EMB_FLAG_* bits raised by kernels.
@@ -60,6 +61,8 @@ struct TableView {
   const SlotInfo* sinfo;    // [n_slots]
   void* W;
   float* ACC;
+  float* Z;                 // FTRL tables: the second state array; else NULL
+  __half* W16;              // master-copy tables: the f16 copy of W; else NULL
   const long long* row_key;
   unsigned int* flags;
 };
@@ -140,6 +143,8 @@ struct emb_table {
   void* W_d = nullptr;      // weights (the f32 master for EMB_F16_MASTER tables)
   void* W16_d = nullptr;    // EMB_F16_MASTER tables: the f16 copy the forward reads
   float* ACC_d = nullptr;
+  float* Z_d = nullptr;     // FTRL tables: z
+  int optimizer = EMB_OPT_ADAGRAD;
   long long* row_key_d = nullptr;
   unsigned int* int_to_ext_d = nullptr;
   unsigned int* ext_to_int_d = nullptr;
@@ -167,6 +172,8 @@ struct emb_table {
     v.sinfo = sinfo_d;
     v.W = W_d;
     v.ACC = ACC_d;
+    v.Z = Z_d;
+    v.W16 = (__half*)W16_d;
     v.row_key = row_key_d;
     v.flags = flags_d;
     return v;

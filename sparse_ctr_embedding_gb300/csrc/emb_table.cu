@@ -62,6 +62,7 @@ static emb_status build_plan(const emb_table_desc* d, const int64_t* keys, int64
     return fail(EMB_ERR_INVALID_ARG, "n_slots must be in [1, 65535] with slot_dim given");
   if (d->wdtype != EMB_F32 && d->wdtype != EMB_F16 && d->wdtype != EMB_F16_MASTER)
     return fail(EMB_ERR_INVALID_ARG, "bad wdtype");
+  if (d->optimizer != EMB_OPT_ADAGRAD && d->optimizer != EMB_OPT_FTRL) return fail(EMB_ERR_INVALID_ARG, "bad optimizer");
   const int vec = d->wdtype == EMB_F32 ? 4 : 8;
   P.n_slots = d->n_slots;
   P.dims.assign(d->slot_dim, d->slot_dim + d->n_slots);
@@ -146,6 +147,7 @@ static emb_status build_plan(const emb_table_desc* d, const int64_t* keys, int64
   st.max_dim = max_dim;
   st.wdtype = (int32_t)P.wdtype;
   st.load_factor = (double)n / (double)cap;
+  for (int s = 0; s < P.n_slots; ++s) st.max_slot_keys = std::max<int64_t>(st.max_slot_keys, count[(size_t)s]);
 
   // sequential insertion in keys-array order; home slots of upcoming keys are
   // prefetched (a pure memory hint: the insertion order is unchanged)
@@ -388,6 +390,7 @@ static void free_table(emb_table* t) {
   cudaFree(t->W_d);
   cudaFree(t->W16_d);
   cudaFree(t->ACC_d);
+  cudaFree(t->Z_d);
   cudaFree(t->row_key_d);
   cudaFree(t->int_to_ext_d);
   cudaFree(t->ext_to_int_d);
@@ -457,6 +460,7 @@ emb_status emb_table_create(const emb_table_desc* desc, const int64_t* keys_h, i
   emb_table* t = new (std::nothrow) emb_table();
   if (!t) return fail(EMB_ERR_OOM, "host allocation failed");
   cudaGetDevice(&t->device);
+  t->optimizer = (int)desc->optimizer;
   t->st = P.st;
   t->sinfo_h = P.sinfo;
   t->uniform_dim = P.ext_elem_off.empty() ? P.dims[0] : 0;
@@ -501,6 +505,12 @@ emb_status emb_table_create(const emb_table_desc* desc, const int64_t* keys_h, i
     } else {
       fill_f32_kernel<<<grid_for((long long)ne, 256), 256, 0, st>>>(t->ACC_d, (long long)ne, desc->acc_init);
       EMB_CUDA(cudaGetLastError());
+    }
+    if (desc->optimizer == EMB_OPT_FTRL) {  // FTRL's z starts at zero (emb_table_import_z sets it)
+      EMB_CUDA(cudaMalloc((void**)&t->Z_d, ne * 4));
+      bytes += ne * 4;
+      t->st.device_bytes = bytes;
+      EMB_CUDA(cudaMemsetAsync(t->Z_d, 0, ne * 4, st));
     }
     EMB_CUDA(cudaStreamSynchronize(st));
     return EMB_OK;
@@ -562,6 +572,26 @@ emb_status emb_table_export(const emb_table* table, int64_t* keys_out, void* val
       if (e != cudaSuccess) return cuda_fail(e, "export keys");
     }
   }
+  EMB_CUDA(cudaStreamSynchronize(st));
+  return EMB_OK;
+}
+
+emb_status emb_table_export_z(const emb_table* table, float* z_out, void* stream) {
+  if (!table || !z_out) return fail(EMB_ERR_INVALID_ARG, "NULL argument");
+  if (!table->Z_d) return fail(EMB_ERR_INVALID_ARG, "not an FTRL table");
+  cudaStream_t st = (cudaStream_t)stream;
+  emb_status r = move_rows(table, z_out, table->Z_d, 4, false, st);
+  if (r != EMB_OK) return r;
+  EMB_CUDA(cudaStreamSynchronize(st));
+  return EMB_OK;
+}
+
+emb_status emb_table_import_z(emb_table* table, const float* z_in, void* stream) {
+  if (!table || !z_in) return fail(EMB_ERR_INVALID_ARG, "NULL argument");
+  if (!table->Z_d) return fail(EMB_ERR_INVALID_ARG, "not an FTRL table");
+  cudaStream_t st = (cudaStream_t)stream;
+  emb_status r = move_rows(table, z_in, table->Z_d, 4, true, st);
+  if (r != EMB_OK) return r;
   EMB_CUDA(cudaStreamSynchronize(st));
   return EMB_OK;
 }

@@ -7,12 +7,25 @@ float32 weight storage, 2e-3 for float16 storage):
                   error is measured against the size of its terms)
   accumulator     |x - r| <= tol * r             (acc is positive)
   weight          |x - r| <= tol * max(|r|, |w_old|)
-The library sums each key's gradient with TwoSum compensation, so the
-per-key gradient is within about one rounding of the exact sum however many
-occurrences the key has, and the update meets the plain relative gates even
-where the gradient terms cancel.  The plain maximum relative error
-|x - r| / |r| is reported next to each gate.  Index work (slots, rows, unique
-keys) and untouched rows are compared bit-exactly.
+These plain gates hold for every element of a key whose gradient terms do not
+cancel much: kappa = A_g / |g| <= KAPPA (A_g = sum of |terms| of the key, g
+their sum).  Where they cancel more, no float32 evaluation can give g to a
+relative 1e-5: each term grad_out * (1/L) is a float32 product, rounded once,
+with 1/L itself a rounded float32, so g carries an error of order u * A_g
+(u = 2^-24) whatever the summation.  The library sums with TwoSum
+compensation (groups of at most 4 products summed plainly, then folded in
+exactly), which bounds the whole error by
+  |dg| <= DG_ULPS * u * A_g + u * |g|
+(3u for the roundings of each term: 1/L, its product with the count of a run
+of equal (row, bag) pairs, and the product with grad_out; 3u for a plain
+4-term group sum; u for the float32 partial of a row cut by a sub-chunk edge;
+DG_ULPS = 8 covers these 7u).  For keys with
+kappa > KAPPA the gates add that bound propagated through the update:
+  accumulator  + 2 |g| dg + dg^2         (acc' = acc + g^2)
+  weight       + lr * dg / sqrt(acc')    (|d/dg (g / sqrt(acc + g^2))| <= 1/sqrt(acc'))
+The plain maximum relative error |x - r| / |r| is reported for both classes.
+Index work (slots, rows, unique keys) and untouched rows are compared
+bit-exactly.
 """
 from __future__ import annotations
 
@@ -49,15 +62,47 @@ def gate(name, x, r, scale, tol):
     return rel
 
 
-def acc_scale(acc_r):
-    """Accumulators are positive: a plain relative gate."""
-    return acc_r.astype(np.float64)
+KAPPA = 16.0       # cancellation A_g / |g| up to which the plain gates apply unchanged
+DG_ULPS = 8.0      # bound on the float32 gradient's error, in units of u * A_g
+U32 = 2.0 ** -24   # float32 unit roundoff
 
 
-def w_scale(w_r, w_old):
+def grad_err(G, Ag):
+    """Per-element bound on |g_gpu - g| for keys whose terms cancel (kappa >
+    KAPPA), 0 elsewhere (see the module docstring)."""
+    G = np.abs(np.asarray(G, dtype=np.float64))
+    Ag = np.asarray(Ag, dtype=np.float64)
+    dg = DG_ULPS * U32 * Ag + U32 * G
+    return np.where(Ag > KAPPA * G, dg, 0.0)
+
+
+def acc_scale(acc_r, G=None, Ag=None, tol=1.0):
+    """Accumulators are positive: a plain relative gate, plus (kappa > KAPPA)
+    the propagated gradient bound expressed in units of tol."""
+    s = acc_r.astype(np.float64)
+    if G is not None:
+        dg = grad_err(G, Ag)
+        s = s + (2 * np.abs(np.asarray(G, np.float64)) * dg + dg * dg) / tol
+    return s
+
+
+def w_scale(w_r, w_old, acc_r=None, G=None, Ag=None, lr=0.0, tol=1.0):
     """Weights: relative to the larger of the new and the old weight (an
-    update can move a weight through zero)."""
-    return np.maximum(np.abs(w_r.astype(np.float64)), np.abs(w_old.astype(np.float64)))
+    update can move a weight through zero), plus (kappa > KAPPA) the
+    propagated gradient bound in units of tol."""
+    s = np.maximum(np.abs(w_r.astype(np.float64)), np.abs(w_old.astype(np.float64)))
+    if G is not None:
+        s = s + lr * grad_err(G, Ag) / np.sqrt(acc_r.astype(np.float64)) / tol
+    return s
+
+
+def split_plain_rel(x, r, G, Ag):
+    """Plain max relative error for elements of keys with kappa <= KAPPA and > KAPPA."""
+    x = np.asarray(x, np.float64)
+    r = np.asarray(r, np.float64)
+    hi = np.asarray(Ag, np.float64) > KAPPA * np.abs(np.asarray(G, np.float64))
+    return (plain_rel(x[~hi], r[~hi]) if (~hi).any() else 0.0,
+            plain_rel(x[hi], r[hi]) if hi.any() else 0.0, int(hi.sum()))
 
 
 def report(key: str, **fields) -> None:
@@ -169,11 +214,13 @@ def check_step(cfg, wl, gs: GpuStep, T: Optional[oracle.Table] = None) -> dict:
     idx = elem_index(eoff, rows_u)
     acc0 = np.full(idx.size, cfg.acc0, dtype=np.float32)
     w_r, acc_r = oracle.adagrad(G, values[idx], acc0, cfg.lr, cfg.eps)
-    rep["acc_gate"] = gate("acc", gs.acc_out[idx], acc_r, acc_scale(acc_r), tol)
-    rep["acc_plain_rel"] = plain_rel(gs.acc_out[idx], acc_r)
+    rep["acc_gate"] = gate("acc", gs.acc_out[idx], acc_r, acc_scale(acc_r, G, Ag, tol), tol)
+    rep["acc_plain_rel"], rep["acc_plain_rel_cancelling"], rep["n_cancelling"] = \
+        split_plain_rel(gs.acc_out[idx], acc_r, G, Ag)
     w_r64 = w_r.astype(np.float64)
-    rep["w_gate"] = gate("weight", gs.values_out[idx].astype(np.float64), w_r64, w_scale(w_r, values[idx]), tol)
-    rep["w_plain_rel"] = plain_rel(gs.values_out[idx], w_r64)
+    rep["w_gate"] = gate("weight", gs.values_out[idx].astype(np.float64), w_r64,
+                         w_scale(w_r, values[idx], acc_r, G, Ag, cfg.lr, tol), tol)
+    rep["w_plain_rel"], rep["w_plain_rel_cancelling"], _ = split_plain_rel(gs.values_out[idx], w_r64, G, Ag)
     rep["max_cancellation"] = float((Ag / np.maximum(np.abs(G), 1e-300)).max()) if G.size else 0.0
     # rows not hit: bit-identical weights and accumulators
     untouched = np.ones(values.size, dtype=bool)

@@ -30,7 +30,9 @@ def test_fingerprint_is_stable():
 
 
 def test_launches_per_step_follow_the_digit_width():
-    # header + recording forward, 5 launches per radix pass, reduce, fixup
-    assert bench.launches_per_step(100_000_000, E.EMB_SORT_DIGIT_BITS) == 2 + 4 * 5 + 2   # 27 bits, 4 passes
-    assert bench.launches_per_step(65_536, E.EMB_SORT_DIGIT_BITS) == 2 + 3 * 5 + 2       # 17 bits, 3 passes
-    assert bench.launches_per_step(100, 7) == 2 + 1 * 5 + 2
+    # placement (4) + recording forward, 5 launches per radix pass, reduce, fixup;
+    # the backward sorts rows within a slot: the largest slot's key count sets the passes
+    assert bench.launches_per_step(1_562_500, E.EMB_SORT_DIGIT_BITS) == 5 + 3 * 5 + 2     # 21 bits, 3 passes
+    assert bench.launches_per_step(16_383, E.EMB_SORT_DIGIT_BITS) == 5 + 2 * 5 + 2        # 14 bits, 2 passes
+    assert bench.launches_per_step(16_384, E.EMB_SORT_DIGIT_BITS) == 5 + 3 * 5 + 2        # 15 bits, 3 passes
+    assert bench.launches_per_step(100, 7) == 5 + 1 * 5 + 2

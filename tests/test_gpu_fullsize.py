@@ -23,7 +23,7 @@ import torch
 import oracle
 import workload as W
 import sparse_ctr_embedding_gb300 as E
-from parity_util import acc_scale, gate, plain_rel, report, tol_of, w_scale
+from parity_util import acc_scale, gate, plain_rel, report, split_plain_rel, tol_of, w_scale
 
 pytestmark = [pytest.mark.gpu, pytest.mark.slow]
 
@@ -177,11 +177,14 @@ def test_adagrad_on_hot_and_sampled_keys(run):
     w_x = wg.cpu().numpy().reshape(-1)[mask].astype(np.float64)
     a_x = ag.cpu().numpy().reshape(-1)[mask]
     tol = tol_of(cfg)
-    ga = gate("acc", a_x, acc_r, acc_scale(acc_r), tol)
-    gw = gate("weight", w_x, w_r.astype(np.float64), w_scale(w_r, vals[idx]), tol)
+    ga = gate("acc", a_x, acc_r, acc_scale(acc_r, G, Ag, tol), tol)
+    gw = gate("weight", w_x, w_r.astype(np.float64), w_scale(w_r, vals[idx], acc_r, G, Ag, cfg.lr, tol), tol)
     cond = float((Ag / np.maximum(np.abs(G), 1e-300)).max())   # A_g / |g|: how much the key's terms cancel
+    ap, apc, ncan = split_plain_rel(a_x, acc_r, G, Ag)
+    wp, wpc, _ = split_plain_rel(w_x, w_r, G, Ag)
     report(f"full/{cfg.name}/{run.path}", keys=int(pick.size), hottest=int(hot.size), acc_gate=ga, w_gate=gw,
-           acc_plain_rel=plain_rel(a_x, acc_r), w_plain_rel=plain_rel(w_x, w_r), max_cancellation=cond)
+           acc_plain_rel=ap, acc_plain_rel_cancelling=apc, w_plain_rel=wp, w_plain_rel_cancelling=wpc,
+           n_cancelling=ncan, n_elems=int(idx.size), max_cancellation=cond)
 
 
 def test_untouched_rows_bit_identical(run):

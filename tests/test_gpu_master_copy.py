@@ -48,9 +48,9 @@ def _check_master_step(cfg, wl, gs):
     acc0 = np.full(idx.size, cfg.acc0, dtype=np.float32)
     w_r, acc_r = oracle.adagrad(G, master0[idx], acc0, cfg.lr, cfg.eps)
     assert gs.values_out.dtype == np.float32                     # export returns the masters
-    gate("accumulators", gs.acc_out[idx], acc_r, acc_scale(acc_r), tol)
+    gate("accumulators", gs.acc_out[idx], acc_r, acc_scale(acc_r, G, Ag, tol), tol)
     gate("master weights", gs.values_out[idx].astype(np.float64), w_r.astype(np.float64),
-         w_scale(w_r, master0[idx]), tol)
+         w_scale(w_r, master0[idx], acc_r, G, Ag, cfg.lr, tol), tol)
     untouched = np.ones(master0.size, dtype=bool)
     untouched[idx] = False
     assert np.array_equal(gs.values_out[untouched].view(np.int32), master0[untouched].view(np.int32))

@@ -388,3 +388,76 @@ def test_master_copy_rows_are_the_masters_rounded_to_nearest_even():
     assert np.array_equal(c.view(np.uint16), m.astype(np.float16).view(np.uint16))
     assert c[-5] == np.float16(1.0) and c[-4] == np.float16(1 + 2.0 ** -9) and c[-3] == np.float16(-1.0)
 
+
+
+# ------------------------------------------------------------------ FTRL-Proximal
+
+def test_ftrl_without_regularisation_is_adagrad():
+    """With lambda1 = lambda2 = 0, FTRL-Proximal with per-coordinate rates
+    eta_t = alpha / (beta + sqrt(n_t)) is online gradient descent with those
+    rates (McMahan et al., KDD 2013, section 3.1: the FTRL-Proximal and OGD
+    updates coincide), i.e. Adagrad with lr = alpha and eps = beta, provided
+    the starting weight is the one z encodes, w_0 = -eta_0 z_0.  So several
+    oracle FTRL steps must follow torch.optim.Adagrad (float64) from that start.
+    A wrong sign, a dropped sigma * w term, or sqrt(n) taken before instead of
+    after the update breaks the agreement."""
+    rng = np.random.default_rng(21)
+    m, alpha, beta, n0 = 4000, 0.05, 0.7, 0.1
+    w0 = rng.uniform(-0.05, 0.05, m).astype(np.float32)
+    z = (-w0.astype(np.float64) * (beta + math.sqrt(n0)) / alpha).astype(np.float32)
+    n = np.full(m, n0, np.float32)
+    w = w0.copy()
+    p = torch.from_numpy(w0.astype(np.float64)).requires_grad_(True)
+    opt = torch.optim.Adagrad([p], lr=alpha, eps=beta, initial_accumulator_value=n0)
+    for step in range(6):
+        g = rng.standard_normal(m) * (0.3 if step % 2 else 2.0)
+        w, n, z = oracle.ftrl(g, w, n, z, alpha, beta, 0.0, 0.0)
+        p.grad = torch.from_numpy(g.astype(np.float32).astype(np.float64))
+        opt.step()
+        ref = p.detach().numpy()
+        np.testing.assert_allclose(w, ref, rtol=2e-5, atol=2e-5 * np.abs(ref).max())
+
+
+def test_ftrl_weight_is_the_proximal_minimiser():
+    """The closed-form weight is the minimiser of the per-coordinate objective
+    z w + lambda1 |w| + (1/2) ((beta + sqrt(n)) / alpha + lambda2) w^2
+    (McMahan et al. 2013, Algorithm 1 and its derivation); checked against a
+    numerical minimisation, which pins the signs and where lambda1 and
+    lambda2 enter.  One step from w = 0 (so z' = z + g exactly)."""
+    from scipy.optimize import minimize_scalar
+    rng = np.random.default_rng(22)
+    alpha, beta, l1, l2 = 0.1, 1.0, 0.4, 0.3
+    m = 300
+    g = rng.standard_normal(m) * 1.5
+    w, n, z = oracle.ftrl(g, np.zeros(m, np.float32), np.full(m, 0.25, np.float32),
+                          rng.standard_normal(m).astype(np.float32), alpha, beta, l1, l2)
+    zeros = 0
+    for i in range(m):
+        q = (beta + math.sqrt(float(n[i]))) / alpha + l2
+        f = lambda x: float(z[i]) * x + l1 * abs(x) + 0.5 * q * x * x
+        r = minimize_scalar(f, bounds=(-50.0, 50.0), method="bounded", options={"xatol": 1e-12})
+        assert abs(float(w[i]) - r.x) <= 1e-6 * max(1.0, abs(r.x)), (i, w[i], r.x)
+        zeros += w[i] == 0
+    assert 0 < zeros < m                         # both branches exercised
+
+
+def test_ftrl_state_invariants():
+    """n accumulates g^2 exactly as the Adagrad accumulator does (same float32
+    operations); with w = 0 the z update is z + g; lambda1 above every |z|
+    makes every weight exactly 0 (the sparsity FTRL-Proximal is used for)."""
+    rng = np.random.default_rng(23)
+    m = 1000
+    G = rng.standard_normal(m)
+    w0 = rng.uniform(-0.05, 0.05, m).astype(np.float32)
+    n0 = np.full(m, 0.1, np.float32)
+    z0 = rng.standard_normal(m).astype(np.float32)
+    _, n1, _ = oracle.ftrl(G, w0, n0, z0, 0.05, 1.0, 0.0, 0.0)
+    _, acc1 = oracle.adagrad(G, w0, n0, 0.05, 1e-8)
+    assert np.array_equal(n1.view(np.uint32), acc1.view(np.uint32))
+    _, _, z1 = oracle.ftrl(G, np.zeros(m, np.float32), n0, z0, 0.05, 1.0, 0.0, 0.0)
+    assert np.array_equal(z1, (z0 + G.astype(np.float32)).astype(np.float32))
+    wbig, _, _ = oracle.ftrl(G, w0, n0, z0, 0.05, 1.0, 1e6, 0.0)
+    assert np.all(wbig == 0)
+    wh, _, _ = oracle.ftrl(G, w0.astype(np.float16), n0, z0, 0.05, 1.0, 0.1, 0.2)
+    wf, _, _ = oracle.ftrl(G, w0.astype(np.float16).astype(np.float32), n0, z0, 0.05, 1.0, 0.1, 0.2)
+    assert wh.dtype == np.float16 and np.array_equal(wh, wf.astype(np.float16))   # half: read exactly, RNE out

@@ -64,10 +64,10 @@ def _oracle_step(cfg, wl):
     keys, off, q = wl.keys.cpu().numpy(), wl.offsets.cpu().numpy(), wl.qkeys.cpu().numpy()
     values, grad = wl.values.cpu().numpy(), wl.grad.cpu().numpy()
     T = oracle.Table(keys, cfg.capacity, cfg.dims)
-    _, rows_u, _, G, _ = T.backward(off, q, cfg.pool, grad)
+    _, rows_u, _, G, Ag = T.backward(off, q, cfg.pool, grad)
     idx = elem_index(T.elem_offsets(), rows_u)
     w_r, acc_r = oracle.adagrad(G, values[idx], np.full(idx.size, cfg.acc0, np.float32), cfg.lr, cfg.eps)
-    return idx, w_r, acc_r
+    return idx, w_r, acc_r, G, Ag
 
 
 def test_large_call_then_smaller_call_in_the_shared_scratch():
@@ -88,11 +88,11 @@ def test_large_call_then_smaller_call_in_the_shared_scratch():
         w_r, a_r = _export(ref, n_el, wl.values.dtype)
         w_x, a_x = _export(new, n_el, wl.values.dtype)
         assert np.array_equal(_bits(w_x), _bits(w_r)) and np.array_equal(_bits(a_x), _bits(a_r)), cfg.name
-        idx, w_o, a_o = _oracle_step(cfg, wl)
+        idx, w_o, a_o, G, Ag = _oracle_step(cfg, wl)
         tol = tol_of(cfg)
-        gate(f"{cfg.name} accumulators", a_x[idx], a_o, acc_scale(a_o), tol)
+        gate(f"{cfg.name} accumulators", a_x[idx], a_o, acc_scale(a_o, G, Ag, tol), tol)
         gate(f"{cfg.name} weights", w_x[idx].astype(np.float64), w_o.astype(np.float64),
-             w_scale(w_o, wl.values.cpu().numpy()[idx]), tol)
+             w_scale(w_o, wl.values.cpu().numpy()[idx], a_o, G, Ag, cfg.lr, tol), tol)
         ref.close()
         new.close()
 
