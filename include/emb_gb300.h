@@ -171,6 +171,25 @@ typedef struct {
 EMB_API emb_status emb_table_create(const emb_table_desc* desc, const int64_t* keys_h, int64_t n_keys,
                             const void* values, const float* acc, void* stream, emb_table** out);
 
+/*
+ * emb_table_create_device -- the same table as emb_table_create, prepared on
+ * the GPU from keys already in device memory (Tencent PCG talk,
+ * "各阶段优化详细介绍": the table is prepared before the pass and flashed to
+ * GPU memory whole; here the preparation itself runs on the GPU).  The slot
+ * layout, row numbering, statistics and errors are exactly those of
+ * emb_table_create on the same keys: keys inserted in keys-array order with
+ * linear probing, reproduced in parallel (sort by home, prefix-max scan of
+ * the first-come-first-served positions, then each run of occupied slots
+ * replayed in keys-array order).
+ *   keys_d   device int64[n_keys]; values and acc as emb_table_create.
+ * Limits: capacity <= 2^32, and no run of occupied slots longer than 4096
+ * (EMB_ERR_UNSUPPORTED otherwise; at load factor 0.5 runs are a few keys
+ * long, only adversarial keys make long ones).  Scratch of about 48 bytes per
+ * key is allocated and freed during the call.  Synchronises `stream`.
+ */
+EMB_API emb_status emb_table_create_device(const emb_table_desc* desc, const int64_t* keys_d, int64_t n_keys,
+                                           const void* values, const float* acc, void* stream, emb_table** out);
+
 /* Free the table and its device memory (the end of a pass, Tencent PCG talk,
  * "各阶段优化详细介绍").  Work queued on it must be complete. */
 EMB_API emb_status emb_table_destroy(emb_table* table);
@@ -391,6 +410,77 @@ EMB_API emb_status emb_table_slots(const emb_table* table, int64_t* slot_key_out
  * by a kernel since the last check (flags_out, if not NULL, receives them).
  */
 EMB_API emb_status emb_check_device_flag(emb_table* table, void* stream, uint32_t* flags_out);
+
+/*
+ * Batch pipeline (Tencent PCG talk, "GPU 训练整体架构": the stages of the
+ * training step run concurrently as a multi-stage pipeline; JD ads article
+ * 3.2.2: sparse updates pipelined with data movement).  The pipeline owns
+ * `depth` buffer sets (CSR batch, optionally grad_out, pooled output,
+ * backward workspace), an upload stream and a download stream; the step runs
+ * on the caller's compute stream.  Per batch, in this order:
+ *   emb_pipeline_submit    copy the host CSR batch (and grad_out, if the
+ *                          pipeline uploads gradients) into a free set on the
+ *                          upload stream; returns a ticket (0, 1, 2, ...).
+ *                          It may run ahead of the step by up to depth - 1
+ *                          batches: that is the overlap.  A set is reused
+ *                          only after its previous batch's backward and
+ *                          download are done (the upload stream waits on the
+ *                          GPU; the host does not block).
+ *   emb_pipeline_forward   the recording forward of that batch on the compute
+ *                          stream, after its upload; pooled output into out_d
+ *                          (or, NULL, the set's own buffer, returned through
+ *                          out_used) and, if out_h is given, copied to out_h
+ *                          on the download stream.
+ *   emb_pipeline_backward_adagrad / _ftrl
+ *                          the recorded backward of that batch with grad_out_d
+ *                          (device) or, NULL, the uploaded grad_out; then the
+ *                          set is released.  Must come before the next
+ *                          batch's forward (the table keeps one recording).
+ *   emb_pipeline_release   instead of a backward: release a forwarded set
+ *                          (forward-only use).
+ *   emb_pipeline_wait      block the host until the batch's backward (or
+ *                          release) and download are done (then out_h holds
+ *                          its pooled output).
+ * Updates are ordered before the next batch's forward, so a pipelined run
+ * gives exactly the results of the same calls made one after the other.
+ * Host buffers should be pinned for the copies to overlap (pageable memory
+ * still works, synchronously).  Not thread-safe: one host thread drives a
+ * pipeline.  Errors: INVALID_ARG (bad sizes, tickets out of order, a set
+ * still held), OOM / CUDA from create.
+ */
+typedef struct emb_pipeline emb_pipeline;
+EMB_API emb_status emb_pipeline_create(emb_table* table, int64_t max_bags, int64_t max_nnz, int depth,
+                                       int upload_grad, void* compute_stream, emb_pipeline** out);
+EMB_API emb_status emb_pipeline_destroy(emb_pipeline* pipe);
+EMB_API emb_status emb_pipeline_submit(emb_pipeline* pipe, const int64_t* offsets_h, int64_t n_bags,
+                                       const int64_t* keys_h, int64_t nnz, const float* grad_out_h,
+                                       int64_t* ticket_out);
+EMB_API emb_status emb_pipeline_forward(emb_pipeline* pipe, int64_t ticket, emb_pool pool, float* out_d,
+                                        float* out_h, float** out_used);
+EMB_API emb_status emb_pipeline_backward_adagrad(emb_pipeline* pipe, int64_t ticket, const float* grad_out_d,
+                                                 float lr, float eps);
+EMB_API emb_status emb_pipeline_backward_ftrl(emb_pipeline* pipe, int64_t ticket, const float* grad_out_d,
+                                              const emb_ftrl_params* params);
+EMB_API emb_status emb_pipeline_release(emb_pipeline* pipe, int64_t ticket);
+EMB_API emb_status emb_pipeline_wait(emb_pipeline* pipe, int64_t ticket);
+
+/*
+ * Fault injection, for tests of the failure paths (no counterpart in the
+ * pages; everything is injected on the host, no kernel is made to fault).
+ *  - emb_debug_fail_device_alloc(after): the next `after` device allocations
+ *    of the library succeed and every one after them fails as out of memory,
+ *    until called again with a negative value (never fail, the default).
+ *    Process-wide.
+ *  - emb_debug_live_device_allocs(): device allocations of the library not
+ *    yet freed (every table holds some; a failed create leaves none).
+ *  - emb_debug_set_probe_bound(table, bound): lower the table's probe bound,
+ *    1 <= bound <= max_cluster + 1, as a corrupted table would have it: a key
+ *    further than `bound` slots from its home then misses and raises
+ *    EMB_FLAG_PROBE_BOUND, and no probe inspects more than `bound` slots.
+ */
+EMB_API emb_status emb_debug_fail_device_alloc(int64_t after);
+EMB_API int64_t emb_debug_live_device_allocs(void);
+EMB_API emb_status emb_debug_set_probe_bound(emb_table* table, int64_t bound);
 
 /* Human-readable status name, and the calling thread's last error message
  * (no counterpart in the pages). */

@@ -20,9 +20,10 @@ from .build import HEADER, LIB_PATH, build
 
 __all__ = [
     "EmbError", "LibraryNotBuilt", "Table", "lib", "declared_symbols",
-    "emb_table_create", "emb_table_destroy", "emb_table_get_stats", "emb_table_plan",
+    "emb_table_create", "emb_table_create_device", "emb_table_destroy", "emb_table_get_stats", "emb_table_plan",
     "emb_lookup_fwd", "emb_lookup_fwd_record", "emb_bwd_adagrad_recorded", "emb_bwd_workspace_size", "emb_bwd_adagrad", "emb_bwd_adagrad_noalloc",
     "emb_bwd_ftrl", "emb_bwd_ftrl_recorded", "emb_table_export_z", "emb_table_import_z",
+    "emb_debug_fail_device_alloc", "emb_debug_live_device_allocs", "emb_debug_set_probe_bound", "Pipeline",
     "emb_bwd_unique_keys", "emb_bwd_phase_events", "EMB_NOALLOC_SCRATCH_BYTES", "EMB_SORT_DIGIT_BITS", "BWD_PHASES",
     "emb_resolve", "emb_table_export", "emb_table_export_rows", "emb_table_slots", "emb_check_device_flag",
     "emb_status_string", "emb_last_error",
@@ -92,6 +93,7 @@ def lib():
         sig = {
             "emb_table_create": [ctypes.POINTER(_Desc), _vp, _i64, _vp, _vp, _vp, ctypes.POINTER(_vp)],
             "emb_table_destroy": [_vp],
+            "emb_table_create_device": [ctypes.POINTER(_Desc), _vp, _i64, _vp, _vp, _vp, ctypes.POINTER(_vp)],
             "emb_table_get_stats": [_vp, ctypes.POINTER(_Stats)],
             "emb_table_plan": [ctypes.POINTER(_Desc), _vp, _i64, ctypes.POINTER(_Stats), _vp, _vp],
             "emb_lookup_fwd": [_vp, _vp, _i64, _vp, _i64, ctypes.c_int, _vp, _vp],
@@ -110,6 +112,16 @@ def lib():
             "emb_bwd_ftrl_recorded": [_vp, _i64, _i64, ctypes.c_int, _vp, ctypes.POINTER(_Ftrl), _vp,
                                       ctypes.c_size_t, _vp],
             "emb_table_export_z": [_vp, _vp, _vp],
+            "emb_debug_fail_device_alloc": [_i64],
+            "emb_pipeline_create": [_vp, _i64, _i64, ctypes.c_int, ctypes.c_int, _vp, ctypes.POINTER(_vp)],
+            "emb_pipeline_destroy": [_vp],
+            "emb_pipeline_submit": [_vp, _vp, _i64, _vp, _i64, _vp, ctypes.POINTER(_i64)],
+            "emb_pipeline_forward": [_vp, _i64, ctypes.c_int, _vp, _vp, ctypes.POINTER(_vp)],
+            "emb_pipeline_backward_adagrad": [_vp, _i64, _vp, ctypes.c_float, ctypes.c_float],
+            "emb_pipeline_backward_ftrl": [_vp, _i64, _vp, ctypes.POINTER(_Ftrl)],
+            "emb_pipeline_release": [_vp, _i64],
+            "emb_pipeline_wait": [_vp, _i64],
+            "emb_debug_set_probe_bound": [_vp, _i64],
             "emb_table_import_z": [_vp, _vp, _vp],
             "emb_resolve": [_vp, _vp, _i64, _vp, _vp, _vp],
             "emb_table_export": [_vp, _vp, _vp, _vp, _vp],
@@ -125,6 +137,8 @@ def lib():
         L.emb_status_string.restype = ctypes.c_char_p
         L.emb_last_error.argtypes = []
         L.emb_last_error.restype = ctypes.c_char_p
+        L.emb_debug_live_device_allocs.argtypes = []
+        L.emb_debug_live_device_allocs.restype = ctypes.c_int64
         _lib = L
     return _lib
 
@@ -221,6 +235,21 @@ def emb_table_create(dims, wdtype: str, keys: torch.Tensor, values: Optional[tor
     _check(lib().emb_table_create(ctypes.byref(d), _ptr(keys, torch.int64, "keys"), keys.numel(),
                                   _ptr(values, wt, "values"), _ptr(acc, torch.float32, "acc"), _stream(stream),
                                   ctypes.byref(h)))
+    return Table(h.value, dims, wdtype, optimizer)
+
+
+def emb_table_create_device(dims, wdtype: str, keys: torch.Tensor, values: Optional[torch.Tensor] = None,
+                            acc: Optional[torch.Tensor] = None, capacity: int = 0, acc_init: float = 0.0,
+                            stream=None, optimizer: str = "adagrad") -> Table:
+    """The table of emb_table_create, prepared on the GPU: keys is a CUDA int64 tensor."""
+    if not keys.is_cuda:
+        raise ValueError("keys must be device memory (emb_table_create takes host keys)")
+    wt = torch.float16 if wdtype == "f16" else torch.float32
+    d, _keep = _desc(dims, wdtype, capacity, acc_init, optimizer)
+    h = _vp()
+    _check(lib().emb_table_create_device(ctypes.byref(d), _cuda(keys, torch.int64, "keys"), keys.numel(),
+                                         _ptr(values, wt, "values"), _ptr(acc, torch.float32, "acc"),
+                                         _stream(stream), ctypes.byref(h)))
     return Table(h.value, dims, wdtype, optimizer)
 
 
@@ -410,3 +439,80 @@ def emb_check_device_flag(table: Table, stream=None) -> int:
     if rc not in (EMB_OK, 8):
         raise EmbError(rc, emb_last_error())
     return f.value
+
+
+def emb_debug_fail_device_alloc(after: int) -> None:
+    """Fault injection: the next `after` device allocations succeed, later ones fail (negative: never)."""
+    _check(lib().emb_debug_fail_device_alloc(int(after)))
+
+
+def emb_debug_live_device_allocs() -> int:
+    return int(lib().emb_debug_live_device_allocs())
+
+
+def emb_debug_set_probe_bound(table: Table, bound: int) -> None:
+    """Fault injection: lower the table's probe bound (as a corrupted table would)."""
+    _check(lib().emb_debug_set_probe_bound(table.handle, int(bound)))
+    table.stats = emb_table_get_stats(table)
+
+
+class Pipeline:
+    """emb_pipeline: overlaps the next batch's host-to-device copy (and the
+    pooled output's copy back) with the current step.  Host tensors should be
+    pinned.  Per batch: submit -> forward -> backward_adagrad/ftrl (or
+    release) -> wait; submit may run up to depth - 1 batches ahead."""
+
+    def __init__(self, table: Table, max_bags: int, max_nnz: int, depth: int = 2, upload_grad: bool = False,
+                 stream=None):
+        self.table = table
+        self._keep = []
+        h = _vp()
+        _check(lib().emb_pipeline_create(table.handle, int(max_bags), int(max_nnz), int(depth), int(upload_grad),
+                                         _stream(stream), ctypes.byref(h)))
+        self._h = h
+
+    def submit(self, offsets_h: torch.Tensor, keys_h: torch.Tensor, grad_h: Optional[torch.Tensor] = None) -> int:
+        for t, n in ((offsets_h, "offsets"), (keys_h, "keys"), (grad_h, "grad_out")):
+            if t is not None and t.is_cuda:
+                raise ValueError(f"{n} must be host memory")
+        tk = ctypes.c_int64()
+        _check(lib().emb_pipeline_submit(self._h, _ptr(offsets_h, torch.int64, "offsets"), offsets_h.numel() - 1,
+                                         _ptr(keys_h, torch.int64, "keys"), keys_h.numel(),
+                                         _ptr(grad_h, torch.float32, "grad_out"), ctypes.byref(tk)))
+        self._keep.append((offsets_h, keys_h, grad_h))   # host memory must outlive the copy
+        self._keep = self._keep[-8:]
+        return tk.value
+
+    def forward(self, ticket: int, pool: str, out: Optional[torch.Tensor] = None,
+                out_h: Optional[torch.Tensor] = None) -> int:
+        """Returns the device address of the pooled output (out, or the set's own buffer)."""
+        used = _vp()
+        _check(lib().emb_pipeline_forward(self._h, int(ticket), _POOL[pool], _ptr(out, torch.float32, "out"),
+                                          _ptr(out_h, torch.float32, "out_h"), ctypes.byref(used)))
+        return used.value
+
+    def backward_adagrad(self, ticket: int, lr: float, eps: float, grad_out: Optional[torch.Tensor] = None):
+        _check(lib().emb_pipeline_backward_adagrad(self._h, int(ticket), _ptr(grad_out, torch.float32, "grad_out"),
+                                                   ctypes.c_float(lr), ctypes.c_float(eps)))
+
+    def backward_ftrl(self, ticket: int, alpha, beta, lambda1, lambda2, grad_out: Optional[torch.Tensor] = None):
+        p = _ftrl(alpha, beta, lambda1, lambda2)
+        _check(lib().emb_pipeline_backward_ftrl(self._h, int(ticket), _ptr(grad_out, torch.float32, "grad_out"),
+                                                ctypes.byref(p)))
+
+    def release(self, ticket: int):
+        _check(lib().emb_pipeline_release(self._h, int(ticket)))
+
+    def wait(self, ticket: int):
+        _check(lib().emb_pipeline_wait(self._h, int(ticket)))
+
+    def close(self):
+        if self._h:
+            lib().emb_pipeline_destroy(self._h)
+            self._h = _vp()
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass

@@ -16,7 +16,7 @@ CSRC = os.path.join(HERE, "csrc")
 BUILD = os.path.join(HERE, "_build")
 LIB_PATH = os.path.join(BUILD, "libemb_gb300.so")
 HEADER = os.path.join(ROOT, "include", "emb_gb300.h")
-SOURCES = ["emb_table.cu", "emb_fwd.cu", "emb_bwd.cu"]
+SOURCES = ["emb_table.cu", "emb_fwd.cu", "emb_bwd.cu", "emb_pipe.cu", "emb_build.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC = os.environ.get("NVCC", "nvcc")
 CFLAGS = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC,-fvisibility=hidden",

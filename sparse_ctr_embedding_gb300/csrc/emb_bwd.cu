@@ -88,7 +88,7 @@ struct SortSeg {
 static size_t align_up(size_t x) { return (x + 255) & ~(size_t)255; }
 
 struct WsLayout {
-  size_t hdr, kA, kB, vA, vB, scale, dest, sseg, counts, partials, partA, partB, arow, zero, work, fwork, uniq, total;
+  size_t hdr, kA, kB, vA, vB, scale, dest, sseg, treg, counts, partials, partA, partB, arow, zero, work, fwork, uniq, total;
   unsigned n_tiles_sort, n_regions, n_chunks, n_scan_partials;
   int max_dim;
 };
@@ -119,6 +119,7 @@ static WsLayout ws_layout(const emb_table* t, long long n_bags, long long nnz) {
   L.scale = take(nb * 4);
   L.dest = take(nb * 4);                                  // first position of each bag's pairs
   L.sseg = take((size_t)(L.n_regions + 1) * sizeof(SortSeg));
+  L.treg = take((size_t)L.n_tiles_sort * 4);              // region of each sort tile
   L.counts = take(n_counts * 4);
   L.partials = take((size_t)(L.n_scan_partials + 1) * 4);
   L.partA = take((size_t)L.n_chunks * L.max_dim * 4);
@@ -142,7 +143,7 @@ __device__ __forceinline__ unsigned lanemask_lt() {
 
 // Unrecorded path: one warp per bag probes its keys and writes the pair
 // (internal row, bag) of every occurrence at the bag's place in the slot-major
-// order (dest[bag], see placement below; row n_rows for a miss, which sorts last
+// order (dest, see placement below; row n_rows for a miss, which sorts last
 // in its slot), and 1/L per bag for mean.
 __global__ void __launch_bounds__(256) expand_kernel(TableView t, const long long* __restrict__ offsets,
                                                      long long n_bags, const long long* __restrict__ keys,
@@ -153,6 +154,7 @@ __global__ void __launch_bounds__(256) expand_kernel(TableView t, const long lon
   const long long gw = (blockIdx.x * (long long)blockDim.x + threadIdx.x) >> 5;
   const long long nwarps = ((long long)gridDim.x * blockDim.x) >> 5;
   const unsigned S = (unsigned)t.n_slots;
+  const unsigned long long B = (unsigned long long)n_bags / S;
   for (long long bag = gw; bag < n_bags; bag += nwarps) {
     const int s = (int)((unsigned)bag % S);
     long long start = offsets[bag], end = offsets[bag + 1];
@@ -162,7 +164,7 @@ __global__ void __launch_bounds__(256) expand_kernel(TableView t, const long lon
       end = min(max(end, start), nnz);
     }
     if (mean && lane == 0) scale[bag] = end > start ? 1.0f / (float)(end - start) : 0.f;
-    const long long d0 = (long long)dest[bag] - start;
+    const long long d0 = (long long)dest[(unsigned long long)s * B + (unsigned long long)bag / S] - start;
     for (long long i = start + lane; i < end; i += 32) {
       const long long k = keys[i];
       unsigned row = t.n_rows, ext;
@@ -243,12 +245,13 @@ __device__ __forceinline__ unsigned region_digit(const SortSeg& g, unsigned k, i
 __global__ void __launch_bounds__(kSortThreads) radix_count_kernel(const unsigned* __restrict__ keys,
                                                                    const SortSeg* __restrict__ sg,
                                                                    unsigned n_regions, int shift,
-                                                                   unsigned* __restrict__ counts) {
+                                                                   unsigned* __restrict__ counts,
+                                                                   const unsigned* __restrict__ tile_reg) {
   __shared__ unsigned cnt[kSortWarps][kDigits];
   __shared__ unsigned reg;
   const int w = threadIdx.x >> 5;
   const unsigned tile = blockIdx.x;
-  if (threadIdx.x == 0) reg = region_of_tile(sg, n_regions, tile);
+  if (threadIdx.x == 0) reg = tile_reg ? tile_reg[tile] : region_of_tile(sg, n_regions, tile);
   for (int i = threadIdx.x; i < kSortWarps * kDigits; i += kSortThreads) (&cnt[0][0])[i] = 0;
   __syncthreads();
   const unsigned r = reg;
@@ -330,7 +333,7 @@ __device__ __forceinline__ unsigned block_excl_scan(unsigned v, unsigned* sm) {
 __global__ void __launch_bounds__(kSortThreads, 3) radix_scatter_kernel(
     const unsigned* __restrict__ kin, const unsigned* __restrict__ vin, unsigned* __restrict__ kout,
     unsigned* __restrict__ vout, int shift, const unsigned* __restrict__ counts, const SortSeg* __restrict__ sg,
-    unsigned n_regions, unsigned miss, unsigned n_bags) {
+    unsigned n_regions, unsigned miss, unsigned n_bags, const unsigned* __restrict__ tile_reg) {
   extern __shared__ unsigned smem[];
   unsigned(*cnt)[kDigits] = reinterpret_cast<unsigned(*)[kDigits]>(smem);  // [kSortWarps][kDigits]
   unsigned* gbase = smem + kSortWarps * kDigits;                             // [kDigits]
@@ -341,7 +344,7 @@ __global__ void __launch_bounds__(kSortThreads, 3) radix_scatter_kernel(
   __shared__ unsigned reg;
   const int w = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const unsigned tile = blockIdx.x;
-  if (threadIdx.x == 0) reg = region_of_tile(sg, n_regions, tile);
+  if (threadIdx.x == 0) reg = tile_reg ? tile_reg[tile] : region_of_tile(sg, n_regions, tile);
   __syncthreads();
   const unsigned r = reg;
   if (r == n_regions) return;  // a spare tile
@@ -499,67 +502,67 @@ __global__ void __launch_bounds__(kScanThreads) scan_down_kernel(const unsigned*
 // numbers: at 64 slots of 1.56M keys 21 bits (3 passes of 7) instead of 27
 // (4 passes), and the occurrences of a row keep the order they had before
 // (the bags of its slot in b order), so the per-row sums are unchanged.
-// dest[bag] is the exclusive prefix sum, in slot-major order (t = s * B + b),
-// of the bag lengths, each clamped exactly as the forward clamps malformed
-// offsets; it is stored by bag (b * S + s), the order the forward walks.
+// dest[t], t = s * B + b, is the exclusive prefix sum of the bag lengths in
+// slot-major order, each clamped exactly as the forward clamps malformed
+// offsets: the first position of bag b * S + s's pairs.
 
-__device__ __forceinline__ unsigned long long bag_len_t(const long long* __restrict__ offsets, size_t t,
-                                                        unsigned long long B, unsigned S, long long nnz) {
-  const unsigned long long s = t / B, b = t % B;
-  const unsigned long long bag = b * S + s;
-  const long long start = min(max(offsets[bag], 0LL), nnz);
-  const long long end = min(max(offsets[bag + 1], start), nnz);
-  return (unsigned long long)(end - start);
+// Bag lengths (clamped as the forward clamps them) in slot-major order:
+// Lt[s * B + b] = length of bag b * S + s.  A 32 x 32 tile of (sample, slot)
+// per block, read along slots (consecutive offsets) and written along
+// samples through shared memory, so both sides are coalesced; each block
+// also adds its exact 64-bit sum of lengths to the header's total (zeroed
+// beforehand), which equals nnz exactly when the clamped bags tile [0, nnz).
+__global__ void __launch_bounds__(256) len_transpose_kernel(const long long* __restrict__ offsets,
+                                                            unsigned long long B, unsigned S, long long nnz,
+                                                            unsigned* __restrict__ Lt, WsHeader* hdr) {
+  __shared__ unsigned tile[32][33];
+  __shared__ unsigned long long wsum[8];
+  const unsigned tx = threadIdx.x & 31, ty = threadIdx.x >> 5;  // 32 x 8 threads
+  const unsigned long long b0 = (unsigned long long)blockIdx.x * 32;
+  const unsigned s0 = blockIdx.y * 32;
+  unsigned long long sum = 0;
+#pragma unroll
+  for (int r = 0; r < 4; ++r) {
+    const unsigned long long b = b0 + ty + 8 * r;
+    const unsigned s = s0 + tx;
+    unsigned len = 0;
+    if (b < B && s < S) {
+      const unsigned long long bag = b * S + s;
+      const long long start = min(max(offsets[bag], 0LL), nnz);
+      const long long end = min(max(offsets[bag + 1], start), nnz);
+      len = (unsigned)(end - start);
+    }
+    tile[ty + 8 * r][tx] = len;
+    sum += len;
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, o);
+  if (tx == 0) wsum[ty] = sum;
+  __syncthreads();
+#pragma unroll
+  for (int r = 0; r < 4; ++r) {
+    const unsigned s = s0 + ty + 8 * r;
+    const unsigned long long b = b0 + tx;
+    if (b < B && s < S) Lt[(unsigned long long)s * B + b] = tile[tx][ty + 8 * r];
+  }
+  if (threadIdx.x == 0) {
+    unsigned long long t = 0;
+    for (int w = 0; w < 8; ++w) t += wsum[w];
+    if (t) atomicAdd(&hdr->total, t);
+  }
 }
 
-// Per-tile sums of the slot-major bag lengths (strided like scan_reduce_kernel),
-// and their exact 64-bit total in the header (zeroed beforehand): it equals
-// nnz exactly when the clamped bags tile [0, nnz).
-__global__ void __launch_bounds__(kScanThreads) len_scan_reduce_kernel(const long long* __restrict__ offsets,
-                                                                       unsigned long long B, unsigned S,
-                                                                       long long nnz, size_t n,
-                                                                       unsigned* __restrict__ partials,
-                                                                       WsHeader* hdr) {
-  __shared__ unsigned wt[33];
-  const size_t base = (size_t)blockIdx.x * kScanTile;
-  unsigned long long s64 = 0;
-#pragma unroll 4
-  for (int j = 0; j < kScanItems; ++j) {
-    const size_t i = base + (size_t)j * kScanThreads + threadIdx.x;
-    if (i < n) s64 += bag_len_t(offsets, i, B, S, nnz);
-  }
-  block_excl_scan((unsigned)s64, wt);
-  if (threadIdx.x == 0) partials[blockIdx.x] = wt[32];
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) s64 += __shfl_xor_sync(0xffffffffu, s64, o);
-  if ((threadIdx.x & 31) == 0 && s64) atomicAdd(&hdr->total, s64);
-}
-
-// dest[bag of t] = exclusive prefix of the slot-major bag lengths (blocked, like scan_down_kernel).
-__global__ void __launch_bounds__(kScanThreads) len_scan_down_kernel(const long long* __restrict__ offsets,
-                                                                     unsigned long long B, unsigned S, long long nnz,
-                                                                     size_t n, unsigned* __restrict__ dest,
-                                                                     const unsigned* __restrict__ partials) {
-  __shared__ unsigned wt[33];
-  const size_t base = (size_t)blockIdx.x * kScanTile + (size_t)threadIdx.x * kScanItems;
-  unsigned v[kScanItems];
-  unsigned s = 0;
-#pragma unroll
-  for (int j = 0; j < kScanItems; ++j) {
-    v[j] = base + j < n ? (unsigned)bag_len_t(offsets, base + j, B, S, nnz) : 0u;
-    s += v[j];
-  }
-  unsigned excl = block_excl_scan(s, wt) + partials[blockIdx.x];
-#pragma unroll
-  for (int j = 0; j < kScanItems; ++j) {
-    if (base + j < n) dest[((base + j) % B) * S + (base + j) / B] = excl;
-    excl += v[j];
-  }
+// The region of every sort tile, found once per step: the largest region r
+// with sg[r].tile0 <= tile, or n_regions for the spare tiles after the last.
+__global__ void tile_map_kernel(const SortSeg* __restrict__ sg, unsigned n_regions, unsigned n_tiles,
+                                unsigned* __restrict__ tile_reg) {
+  for (unsigned t = blockIdx.x * blockDim.x + threadIdx.x; t < n_tiles; t += gridDim.x * blockDim.x)
+    tile_reg[t] = region_of_tile(sg, n_regions, t);
 }
 
 // One block: the workspace header and the sort regions.  Region s < S holds
-// slot s's pairs, from the first position of its first bag (bag s, sample 0)
-// to that of slot s + 1 (the last slot ends at nnz); region S, the absent
+// slot s's pairs, [dest[s * B], dest[(s + 1) * B]) (the last slot ends at
+// nnz); region S, the absent
 // region, is empty.  If the clamped bag lengths do not add up to nnz
 // (malformed offsets; flagged) the bags do not tile [0, nnz): then every
 // slot region is empty and the absent region covers all of [0, nnz), so the
@@ -590,8 +593,8 @@ __global__ void __launch_bounds__(1024) seg_setup_kernel(TableView t, WsHeader* 
     unsigned nt = 0;
     if (r < S) {
       if (placed) {
-        g.lo = dest[r];
-        g.hi = r + 1 < S ? dest[r + 1] : nnz;
+        g.lo = dest[(unsigned long long)r * B];
+        g.hi = r + 1 < S ? dest[(unsigned long long)(r + 1) * B] : nnz;
       }
       const SlotInfo si = t.sinfo[r];
       g.rbase = si.row_base;
@@ -885,7 +888,7 @@ __device__ __forceinline__ void fma_vw(float* acc, float w, const float* g) {
 
 // kAllCols: every lane column is inside every row (one dim, equal to G x VW x NCB).
 template <typename TW, int G, int VW, int NCB, int U, bool kAllCols, typename Opt>
-__global__ void __launch_bounds__(kRedWarps * 32, 10) segreduce_update_kernel(
+__global__ void __launch_bounds__(kRedWarps * 32, 8) segreduce_update_kernel(
     TableView t, const unsigned* __restrict__ K, const unsigned* __restrict__ V, const float* __restrict__ scale,
     int mean, const float* __restrict__ grad, const float* __restrict__ zrow, unsigned n, unsigned n_bags,
     unsigned n_chunks, float* __restrict__ partA, float* __restrict__ partB, unsigned* __restrict__ arow, Opt opt,
@@ -1218,6 +1221,10 @@ static cudaError_t launch_scan(const unsigned* in, unsigned* out, size_t n, unsi
   return cudaGetLastError();
 }
 
+cudaError_t launch_scan_u32(const unsigned* in, unsigned* out, size_t n, unsigned* partials, cudaStream_t st) {
+  return launch_scan(in, out, n, partials, st);
+}
+
 static size_t scatter_smem() {
   return sizeof(unsigned) * ((size_t)kSortWarps * kDigits + 2 * kDigits + 33 + 2 * (size_t)kSortTile);
 }
@@ -1290,6 +1297,56 @@ static cudaError_t dispatch_reduce(const emb_table* t, const unsigned* K, const 
 #undef EMB_RED
 }
 
+// ------------------------------------------------------------------ stable pair sort for the device table build
+//
+// The same radix kernels over one region [0, n) with no clamping: sorts the
+// pairs (key, value) by the low `bits` bits of key, stably.  Scratch layout:
+// two region entries + digit counts + scan partials.
+
+static size_t pair_sort_counts(unsigned n) { return (size_t)kDigits * ((n + kSortTile - 1) / kSortTile + 2); }
+
+size_t pair_sort_scratch_bytes(unsigned n) {
+  const size_t nc = pair_sort_counts(n);
+  const size_t np = (nc + kScanTile - 1) / kScanTile + 1;
+  return align_up(3 * sizeof(SortSeg)) + align_up(nc * 4) + align_up(np * 4);
+}
+
+__global__ void pair_region_kernel(SortSeg* sg, unsigned n) {
+  const unsigned nt = (n + kSortTile - 1) / kSortTile;
+  sg[0] = SortSeg{0u, n, 0u, 0u, 0xFFFFFFFFu, 0u, 0u, 0u};
+  sg[1] = SortSeg{n, n, nt, 0u, 0u, 1u, 0u, 0u};
+  sg[2] = SortSeg{0u, 0u, nt, 0u, 0u, 0u, 0u, 0u};
+}
+
+// Sorted pairs end in (kA, vA) if the pass count is even, else (kB, vB); *in_b says which.
+cudaError_t pair_sort(unsigned* kA, unsigned* vA, unsigned* kB, unsigned* vB, unsigned n, int bits, void* scratch,
+                      cudaStream_t st, bool* in_b) {
+  *in_b = false;
+  if (n == 0) return cudaSuccess;
+  char* sc = (char*)scratch;
+  SortSeg* sg = (SortSeg*)sc;
+  const size_t nc = pair_sort_counts(n);
+  unsigned* counts = (unsigned*)(sc + align_up(3 * sizeof(SortSeg)));
+  unsigned* partials = (unsigned*)(sc + align_up(3 * sizeof(SortSeg)) + align_up(nc * 4));
+  const unsigned n_tiles = (unsigned)(nc / kDigits);
+  pair_region_kernel<<<1, 1, 0, st>>>(sg, n);
+  const size_t smem = scatter_smem();
+  cudaError_t e = cudaFuncSetAttribute(radix_scatter_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  if (e != cudaSuccess) return e;
+  const int passes = std::max(1, (bits + kRadixBits - 1) / kRadixBits);
+  unsigned *ki = kA, *vi = vA, *ko = kB, *vo = vB;
+  for (int p = 0; p < passes; ++p) {
+    radix_count_kernel<<<n_tiles, kSortThreads, 0, st>>>(ki, sg, 1u, p * kRadixBits, counts, nullptr);
+    if ((e = launch_scan(counts, counts, nc, partials, st)) != cudaSuccess) return e;
+    radix_scatter_kernel<<<n_tiles, kSortThreads, smem, st>>>(ki, vi, ko, vo, p * kRadixBits, counts, sg, 1u, 0u, 0u,
+                                                             nullptr);
+    std::swap(ki, ko);
+    std::swap(vi, vo);
+  }
+  *in_b = (passes & 1) != 0;
+  return cudaGetLastError();
+}
+
 static int bits_for(unsigned x) {
   int b = 0;
   while (b < 32 && (x >> b) != 0) ++b;
@@ -1310,19 +1367,19 @@ static emb_status launch_placement(const emb_table* t, const int64_t* offsets_d,
   WsHeader* hdr = (WsHeader*)(ws + L.hdr);
   unsigned* dest = (unsigned*)(ws + L.dest);
   unsigned* partials = (unsigned*)(ws + L.partials);
+  SortSeg* sg = (SortSeg*)(ws + L.sseg);
   const unsigned S = (unsigned)t->st.n_slots;
   const unsigned long long B = (unsigned long long)n_bags / S;
   EMB_CUDA(cudaMemsetAsync(&hdr->total, 0, sizeof(unsigned long long), st));
   if (n_bags > 0) {
-    const unsigned np = (unsigned)((n_bags + kScanTile - 1) / kScanTile);
-    len_scan_reduce_kernel<<<np, kScanThreads, 0, st>>>((const long long*)offsets_d, B, S, nnz, (size_t)n_bags,
-                                                         partials, hdr);
-    scan_partials_kernel<<<1, 1024, 0, st>>>(partials, np);
-    len_scan_down_kernel<<<np, kScanThreads, 0, st>>>((const long long*)offsets_d, B, S, nnz, (size_t)n_bags, dest,
-                                                       partials);
+    const dim3 grid((unsigned)((B + 31) / 32), (S + 31) / 32);
+    len_transpose_kernel<<<grid, 256, 0, st>>>((const long long*)offsets_d, B, S, nnz, dest, hdr);
+    EMB_CUDA(launch_scan(dest, dest, (size_t)n_bags, partials, st));
   }
   seg_setup_kernel<<<1, 1024, 0, st>>>(t->view(), hdr, (unsigned)nnz, (unsigned long long)n_bags,
-                                       (unsigned)(sort_passes(t) & 1), dest, (SortSeg*)(ws + L.sseg));
+                                       (unsigned)(sort_passes(t) & 1), dest, sg);
+  tile_map_kernel<<<(L.n_tiles_sort + 255) / 256, 256, 0, st>>>(sg, L.n_regions, L.n_tiles_sort,
+                                                               (unsigned*)(ws + L.treg));
   EMB_CUDA(cudaGetLastError());
   return EMB_OK;
 }
@@ -1375,12 +1432,13 @@ static emb_status run_bwd(emb_table* table, const int64_t* offsets_d, int64_t n_
   EMB_CUDA(cudaFuncSetAttribute(radix_scatter_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem));
   unsigned *ki = kA, *vi = vA, *ko = kB, *vo = vB;
   const SortSeg* sg = (const SortSeg*)(ws + L.sseg);
+  const unsigned* treg = (const unsigned*)(ws + L.treg);
   for (int p = 0; p < passes; ++p) {
     const int shift = p * kRadixBits;
-    radix_count_kernel<<<L.n_tiles_sort, kSortThreads, 0, st>>>(ki, sg, L.n_regions, shift, counts);
+    radix_count_kernel<<<L.n_tiles_sort, kSortThreads, 0, st>>>(ki, sg, L.n_regions, shift, counts, treg);
     EMB_CUDA(launch_scan(counts, counts, (size_t)kDigits * L.n_tiles_sort, partials, st));
     radix_scatter_kernel<<<L.n_tiles_sort, kSortThreads, smem, st>>>(ki, vi, ko, vo, shift, counts, sg, L.n_regions,
-                                                                     (unsigned)table->st.n_keys, (unsigned)n_bags);
+                                                                     (unsigned)table->st.n_keys, (unsigned)n_bags, treg);
     EMB_CUDA(cudaGetLastError());
     std::swap(ki, ko);
     std::swap(vi, vo);

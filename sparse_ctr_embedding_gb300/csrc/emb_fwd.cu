@@ -16,6 +16,7 @@
 // shuffles and group 0 writes the pooled row with 16-byte stores.
 // Accumulation is float32 in a fixed order, so results are deterministic.
 #include <algorithm>
+#include <cmath>
 
 #include "emb_internal.cuh"
 
@@ -79,7 +80,8 @@ struct Record {
   unsigned* K;
   unsigned* V;
   float* scale;
-  const unsigned* dest;      // per bag: first position of its pairs in slot-major order
+  const unsigned* dest;      // first position of each bag's pairs, slot-major: dest[s * B + b]
+  unsigned long long B;      // samples in the batch
   unsigned long long* work;  // optional bag counter: bags taken in batches, in order
 };
 
@@ -143,7 +145,7 @@ __global__ void __launch_bounds__(256, 8) fwd_pool_kernel(TableView t, const lon
       end = min(max(end, start), nnz);
     }
     // where this bag's pairs go (inside [0, nnz) unless the offsets are malformed)
-    const long long d0 = kRecord ? (long long)rec.dest[bag] - start : 0;
+    const long long d0 = kRecord ? (long long)rec.dest[(unsigned long long)s * rec.B + (unsigned long long)b] - start : 0;
     float acc[NCB][VEC];
 #pragma unroll
     for (int c = 0; c < NCB; ++c)
@@ -228,18 +230,23 @@ __global__ void __launch_bounds__(256, 8) fwd_pool_kernel(TableView t, const lon
   }
 }
 
-// Lanes per bag.  Teams of 8 or 16 lanes (several short bags per warp) were
-// measured slower than one bag per warp at 100M keys x dim 128 (the probes of
-// 32 keys in flight per bag matter more than idle lanes on short bags), so
-// every table uses 32; the narrower teams stay available to the launcher.
-static int fwd_team(int /*max_vecs*/) { return 32; }
+// Lanes per bag: enough for the widest row's 16-byte vectors and for the
+// mean bag's keys to be probed at once, at least 8 and at most a warp.
+// Measured: 100 slots x dim 32 f16 with 5.5-key bags, 8 lanes 2.32 ms against
+// 4.40 ms for a warp per bag; 26 slots x dim 64 f32 with 10.5-key bags, 16
+// lanes 0.388 ms against 0.419; the 100M-key workload (33.7-key bags) and
+// the ragged one (rows up to 32 vectors) keep a whole warp.
+static int fwd_team(int max_vecs, double mean_len) {
+  const int want = std::max(max_vecs, (int)std::ceil(mean_len));
+  return want <= 8 ? 8 : want <= 16 ? 16 : 32;
+}
 
 template <typename TW, bool kRecord>
 static cudaError_t launch_fwd(const emb_table* t, const long long* offsets, long long n_bags, const long long* keys,
                               long long nnz, int mean, float* out, Record rec, cudaStream_t st) {
   constexpr int VEC = VecOf<TW>::kElems;
   const int max_vecs = t->st.max_dim / VEC;  // 16-byte vectors in the widest row
-  const int team = fwd_team(max_vecs);
+  const int team = fwd_team(max_vecs, n_bags > 0 ? (double)nnz / (double)n_bags : 0.0);
   const int ncb = (max_vecs + team - 1) / team;  // column blocks per lane
   const int threads = 256;
   const long long want = std::max(1LL, (n_bags * team + threads - 1) / threads);
@@ -272,7 +279,7 @@ static cudaError_t launch_fwd(const emb_table* t, const long long* offsets, long
 cudaError_t launch_forward(const emb_table* t, const long long* offsets, long long n_bags, const long long* keys,
                            long long nnz, int mean, float* out, unsigned* K, unsigned* V, float* scale,
                            const unsigned* dest, unsigned long long* work, cudaStream_t st) {
-  const Record rec{K, V, scale, dest, work};
+  const Record rec{K, V, scale, dest, (unsigned long long)n_bags / (unsigned long long)t->st.n_slots, work};
   const bool record = K != nullptr;
   if (t->fwd_half())
     return record ? launch_fwd<__half, true>(t, offsets, n_bags, keys, nnz, mean, out, rec, st)

@@ -193,6 +193,20 @@ namespace emb {
 emb_status fail(emb_status s, const std::string& msg);
 emb_status cuda_fail(cudaError_t e, const char* what);
 int sm_count();
+// every device allocation of the library (counted; see emb_debug_fail_device_alloc)
+cudaError_t dmalloc(void** p, size_t bytes);
+void dfree(void* p);
+// table creation steps shared by the host and the device build (emb_table.cu)
+emb_status check_desc(const emb_table_desc* d, int64_t n, int64_t* cap_out, int* max_dim_out,
+                      long long* sum_dims_out);
+emb_status finish_table(emb_table* t, const emb_table_desc* desc, const void* values, const float* acc,
+                        cudaStream_t st, uint64_t* bytes_io);
+void free_table(emb_table* t);
+// sort and scan building blocks (emb_bwd.cu)
+size_t pair_sort_scratch_bytes(unsigned n);
+cudaError_t pair_sort(unsigned* kA, unsigned* vA, unsigned* kB, unsigned* vB, unsigned n, int bits, void* scratch,
+                      cudaStream_t st, bool* in_b);
+cudaError_t launch_scan_u32(const unsigned* in, unsigned* out, size_t n, unsigned* partials, cudaStream_t st);
 }  // namespace emb
 
 #define EMB_CUDA(call)                                        \

@@ -7,6 +7,7 @@
 // GPU never inserts.  Keys follow the unified layout of the same talk
 // ("计算优化"): slot id in the high 16 bits, raw feature id in the low 48.
 #include <algorithm>
+#include <atomic>
 #include <cstdio>
 #include <cstring>
 #include <mutex>
@@ -38,6 +39,36 @@ int sm_count() {
   return n > 0 ? n : 1;
 }
 
+// ------------------------------------------------------------------ device allocations
+//
+// Every device allocation of the library goes through dmalloc/dfree, which
+// count the live ones and can be told (emb_debug_fail_device_alloc) to fail
+// from the N-th call on, so tests can check that a failed create returns
+// EMB_ERR_OOM and leaves nothing allocated.
+
+static std::atomic<long long> g_live_allocs{0};
+static std::atomic<long long> g_fail_after{-1};  // < 0: never fail
+
+cudaError_t dmalloc(void** p, size_t bytes) {
+  long long left = g_fail_after.load();
+  while (left >= 0) {
+    if (left == 0) {
+      *p = nullptr;
+      return cudaErrorMemoryAllocation;
+    }
+    if (g_fail_after.compare_exchange_weak(left, left - 1)) break;
+  }
+  cudaError_t e = cudaMalloc(p, bytes);
+  if (e == cudaSuccess) g_live_allocs.fetch_add(1);
+  return e;
+}
+
+void dfree(void* p) {
+  if (!p) return;
+  cudaFree(p);
+  g_live_allocs.fetch_sub(1);
+}
+
 static unsigned long long host_fmix64(unsigned long long k) {
   k ^= k >> 33;
   k *= 0xff51afd7ed558ccdULL;
@@ -53,10 +84,12 @@ static unsigned long long host_fmix64(unsigned long long k) {
 // slot-major (stable within a slot, i.e. in keys-array order); slots are
 // filled by inserting keys one by one in keys-array order with linear
 // probing, so the layout depends on that order alone.
-static emb_status build_plan(const emb_table_desc* d, const int64_t* keys, int64_t n, HostPlan& P,
-                             bool with_slots) {
+// Validate a table description for n keys: dims, types and the capacity
+// (0 = the smallest power of two >= 2 n).
+emb_status check_desc(const emb_table_desc* d, int64_t n, int64_t* cap_out, int* max_dim_out,
+                      long long* sum_dims_out) {
   if (!d) return fail(EMB_ERR_INVALID_ARG, "desc is NULL");
-  if (n < 0 || (n > 0 && !keys)) return fail(EMB_ERR_INVALID_ARG, "keys is NULL or n_keys < 0");
+  if (n < 0) return fail(EMB_ERR_INVALID_ARG, "n_keys < 0");
   if (n > EMB_MAX_KEYS) return fail(EMB_ERR_UNSUPPORTED, "n_keys exceeds EMB_MAX_KEYS");
   if (d->n_slots < 1 || d->n_slots > 65535 || !d->slot_dim)
     return fail(EMB_ERR_INVALID_ARG, "n_slots must be in [1, 65535] with slot_dim given");
@@ -64,13 +97,10 @@ static emb_status build_plan(const emb_table_desc* d, const int64_t* keys, int64
     return fail(EMB_ERR_INVALID_ARG, "bad wdtype");
   if (d->optimizer != EMB_OPT_ADAGRAD && d->optimizer != EMB_OPT_FTRL) return fail(EMB_ERR_INVALID_ARG, "bad optimizer");
   const int vec = d->wdtype == EMB_F32 ? 4 : 8;
-  P.n_slots = d->n_slots;
-  P.dims.assign(d->slot_dim, d->slot_dim + d->n_slots);
-  P.wdtype = d->wdtype;
   int max_dim = 0;
   long long sum_dims = 0;
-  for (int s = 0; s < P.n_slots; ++s) {
-    int D = P.dims[s];
+  for (int s = 0; s < d->n_slots; ++s) {
+    int D = d->slot_dim[s];
     if (D < 1 || D > EMB_MAX_DIM) return fail(EMB_ERR_UNSUPPORTED, "slot dim outside [1, EMB_MAX_DIM]");
     if (D % vec) return fail(EMB_ERR_UNSUPPORTED, "slot dim must be a multiple of 4 (f32) or 8 (f16)");
     max_dim = std::max(max_dim, D);
@@ -85,6 +115,23 @@ static emb_status build_plan(const emb_table_desc* d, const int64_t* keys, int64
     return fail(EMB_ERR_LOAD_FACTOR, "capacity must be a power of two >= 2 * n_keys");
   }
   if (cap > (1LL << 40)) return fail(EMB_ERR_UNSUPPORTED, "capacity too large");
+  *cap_out = cap;
+  *max_dim_out = max_dim;
+  *sum_dims_out = sum_dims;
+  return EMB_OK;
+}
+
+static emb_status build_plan(const emb_table_desc* d, const int64_t* keys, int64_t n, HostPlan& P,
+                             bool with_slots) {
+  int64_t cap = 0;
+  int max_dim = 0;
+  long long sum_dims = 0;
+  emb_status rc0 = check_desc(d, n, &cap, &max_dim, &sum_dims);
+  if (rc0 != EMB_OK) return rc0;
+  if (n > 0 && !keys) return fail(EMB_ERR_INVALID_ARG, "keys is NULL");
+  P.n_slots = d->n_slots;
+  P.dims.assign(d->slot_dim, d->slot_dim + d->n_slots);
+  P.wdtype = d->wdtype;
   P.n_keys = n;
   P.cap = cap;
 
@@ -322,7 +369,7 @@ static emb_status move_rows(const emb_table* t, const void* user,
   const bool dev = is_device_ptr(user);
   const long long kStageElems = 32LL << 20;
   void* stage = nullptr;
-  if (!dev) EMB_CUDA(cudaMalloc(&stage, (size_t)std::min<long long>(kStageElems, t->st.n_elems) * esz));
+  if (!dev) EMB_CUDA(dmalloc(&stage, (size_t)std::min<long long>(kStageElems, t->st.n_elems) * esz));
   emb_status rc = EMB_OK;
   TableView v = t->view();
   const std::vector<long long>& ext_off_h = t->ext_elem_off_h;
@@ -378,33 +425,79 @@ static emb_status move_rows(const emb_table* t, const void* user,
   }
   if (stage) {
     cudaStreamSynchronize(st);
-    cudaFree(stage);
+    dfree(stage);
   }
   return rc;
 }
 
-static void free_table(emb_table* t) {
+void free_table(emb_table* t) {
   if (!t) return;
-  cudaFree(t->slots_d);
-  cudaFree(t->sinfo_d);
-  cudaFree(t->W_d);
-  cudaFree(t->W16_d);
-  cudaFree(t->ACC_d);
-  cudaFree(t->Z_d);
-  cudaFree(t->row_key_d);
-  cudaFree(t->int_to_ext_d);
-  cudaFree(t->ext_to_int_d);
-  cudaFree(t->ext_elem_off_d);
-  cudaFree(t->flags_d);
+  dfree(t->slots_d);
+  dfree(t->sinfo_d);
+  dfree(t->W_d);
+  dfree(t->W16_d);
+  dfree(t->ACC_d);
+  dfree(t->Z_d);
+  dfree(t->row_key_d);
+  dfree(t->int_to_ext_d);
+  dfree(t->ext_to_int_d);
+  dfree(t->ext_elem_off_d);
+  dfree(t->flags_d);
   delete t;
 }
 
 template <typename T>
-static emb_status dalloc_copy(T** dst, const T* src, size_t count, cudaStream_t st, uint64_t* bytes) {
+emb_status dalloc_copy(T** dst, const T* src, size_t count, cudaStream_t st, uint64_t* bytes) {
   size_t b = std::max<size_t>(count, 1) * sizeof(T);
-  EMB_CUDA(cudaMalloc((void**)dst, b));
+  EMB_CUDA(dmalloc((void**)dst, b));
   *bytes += b;
   if (src && count) EMB_CUDA(cudaMemcpyAsync(*dst, src, count * sizeof(T), cudaMemcpyHostToDevice, st));
+  return EMB_OK;
+}
+
+// The part of table creation after the slot layout and the row maps are on
+// the device: the flag word, weights (from values, in keys-array order, or
+// zeros), the f16 copy of master-copy tables, accumulators (acc or
+// desc->acc_init) and FTRL's z; synchronises the stream.
+emb_status finish_table(emb_table* t, const emb_table_desc* desc, const void* values, const float* acc,
+                        cudaStream_t st, uint64_t* bytes_io) {
+  uint64_t& bytes = *bytes_io;
+  emb_status r;
+  const size_t esz = t->st.wdtype == EMB_F16 ? 2 : 4;
+  if ((r = dalloc_copy(&t->flags_d, (const unsigned*)nullptr, 1, st, &bytes)) != EMB_OK) return r;
+  EMB_CUDA(cudaMemsetAsync(t->flags_d, 0, sizeof(unsigned), st));
+  const size_t ne = (size_t)std::max<long long>(t->st.n_elems, 1);
+  EMB_CUDA(dmalloc(&t->W_d, ne * esz));
+  bytes += ne * esz;
+  EMB_CUDA(dmalloc((void**)&t->ACC_d, ne * 4));
+  bytes += ne * 4;
+  t->st.device_bytes = bytes;
+  if (values) {
+    if ((r = move_rows(t, values, t->W_d, esz, true, st)) != EMB_OK) return r;
+  } else {
+    EMB_CUDA(cudaMemsetAsync(t->W_d, 0, ne * esz, st));
+  }
+  if (t->st.wdtype == EMB_F16_MASTER) {  // W holds the f32 master; the forward reads its f16 copy
+    EMB_CUDA(dmalloc(&t->W16_d, ne * 2));
+    bytes += ne * 2;
+    t->st.device_bytes = bytes;
+    half_copy_kernel<<<grid_for((long long)ne, 256), 256, 0, st>>>((const float*)t->W_d, (__half*)t->W16_d,
+                                                                   (long long)ne);
+    EMB_CUDA(cudaGetLastError());
+  }
+  if (acc) {
+    if ((r = move_rows(t, acc, t->ACC_d, 4, true, st)) != EMB_OK) return r;
+  } else {
+    fill_f32_kernel<<<grid_for((long long)ne, 256), 256, 0, st>>>(t->ACC_d, (long long)ne, desc->acc_init);
+    EMB_CUDA(cudaGetLastError());
+  }
+  if (desc->optimizer == EMB_OPT_FTRL) {  // FTRL's z starts at zero (emb_table_import_z sets it)
+    EMB_CUDA(dmalloc((void**)&t->Z_d, ne * 4));
+    bytes += ne * 4;
+    t->st.device_bytes = bytes;
+    EMB_CUDA(cudaMemsetAsync(t->Z_d, 0, ne * 4, st));
+  }
+  EMB_CUDA(cudaStreamSynchronize(st));
   return EMB_OK;
 }
 
@@ -465,7 +558,6 @@ emb_status emb_table_create(const emb_table_desc* desc, const int64_t* keys_h, i
   t->sinfo_h = P.sinfo;
   t->uniform_dim = P.ext_elem_off.empty() ? P.dims[0] : 0;
   t->ext_elem_off_h.swap(P.ext_elem_off);
-  const size_t esz = P.wdtype == EMB_F16 ? 2 : 4;
   uint64_t bytes = 0;
   auto body = [&]() -> emb_status {
     emb_status r;
@@ -479,41 +571,7 @@ emb_status emb_table_create(const emb_table_desc* desc, const int64_t* keys_h, i
         (r = dalloc_copy(&t->ext_elem_off_d, (const long long*)t->ext_elem_off_h.data(), t->ext_elem_off_h.size(), st,
                          &bytes)) != EMB_OK)
       return r;
-    if ((r = dalloc_copy(&t->flags_d, (const unsigned*)nullptr, 1, st, &bytes)) != EMB_OK) return r;
-    EMB_CUDA(cudaMemsetAsync(t->flags_d, 0, sizeof(unsigned), st));
-    const size_t ne = (size_t)std::max<long long>(t->st.n_elems, 1);
-    EMB_CUDA(cudaMalloc(&t->W_d, ne * esz));
-    bytes += ne * esz;
-    EMB_CUDA(cudaMalloc((void**)&t->ACC_d, ne * 4));
-    bytes += ne * 4;
-    t->st.device_bytes = bytes;
-    if (values) {
-      if ((r = move_rows(t, values, t->W_d, esz, true, st)) != EMB_OK) return r;
-    } else {
-      EMB_CUDA(cudaMemsetAsync(t->W_d, 0, ne * esz, st));
-    }
-    if (P.wdtype == EMB_F16_MASTER) {  // W holds the f32 master; the forward reads its f16 copy
-      EMB_CUDA(cudaMalloc(&t->W16_d, ne * 2));
-      bytes += ne * 2;
-      t->st.device_bytes = bytes;
-      half_copy_kernel<<<grid_for((long long)ne, 256), 256, 0, st>>>((const float*)t->W_d, (__half*)t->W16_d,
-                                                                     (long long)ne);
-      EMB_CUDA(cudaGetLastError());
-    }
-    if (acc) {
-      if ((r = move_rows(t, acc, t->ACC_d, 4, true, st)) != EMB_OK) return r;
-    } else {
-      fill_f32_kernel<<<grid_for((long long)ne, 256), 256, 0, st>>>(t->ACC_d, (long long)ne, desc->acc_init);
-      EMB_CUDA(cudaGetLastError());
-    }
-    if (desc->optimizer == EMB_OPT_FTRL) {  // FTRL's z starts at zero (emb_table_import_z sets it)
-      EMB_CUDA(cudaMalloc((void**)&t->Z_d, ne * 4));
-      bytes += ne * 4;
-      t->st.device_bytes = bytes;
-      EMB_CUDA(cudaMemsetAsync(t->Z_d, 0, ne * 4, st));
-    }
-    EMB_CUDA(cudaStreamSynchronize(st));
-    return EMB_OK;
+    return finish_table(t, desc, values, acc, st, &bytes);
   };
   rc = body();
   if (rc != EMB_OK) {
@@ -563,12 +621,12 @@ emb_status emb_table_export(const emb_table* table, int64_t* keys_out, void* val
       EMB_CUDA(cudaGetLastError());
     } else {
       long long* tmp = nullptr;
-      EMB_CUDA(cudaMalloc((void**)&tmp, (size_t)n * 8));
+      EMB_CUDA(dmalloc((void**)&tmp, (size_t)n * 8));
       export_keys_kernel<<<grid_for(n, 256), 256, 0, st>>>(table->row_key_d, table->ext_to_int_d, 0, n, tmp);
       cudaError_t e = cudaGetLastError();
       if (e == cudaSuccess) e = cudaMemcpyAsync(keys_out, tmp, (size_t)n * 8, cudaMemcpyDeviceToHost, st);
       if (e == cudaSuccess) e = cudaStreamSynchronize(st);
-      cudaFree(tmp);
+      dfree(tmp);
       if (e != cudaSuccess) return cuda_fail(e, "export keys");
     }
   }
@@ -630,7 +688,7 @@ emb_status emb_table_slots(const emb_table* table, int64_t* slot_key_out, int64_
   }
   const long long chunk = 16LL << 20;
   long long* tmp = nullptr;
-  EMB_CUDA(cudaMalloc((void**)&tmp, (size_t)std::min(chunk, cap) * 16));
+  EMB_CUDA(dmalloc((void**)&tmp, (size_t)std::min(chunk, cap) * 16));
   cudaError_t e = cudaSuccess;
   for (long long p0 = 0; p0 < cap && e == cudaSuccess; p0 += chunk) {
     long long p1 = std::min(cap, p0 + chunk), m = p1 - p0;
@@ -642,8 +700,22 @@ emb_status emb_table_slots(const emb_table* table, int64_t* slot_key_out, int64_
       e = cudaMemcpyAsync(slot_row_out + p0, tmp + m, (size_t)m * 8, cudaMemcpyDefault, st);
     if (e == cudaSuccess) e = cudaStreamSynchronize(st);
   }
-  cudaFree(tmp);
+  dfree(tmp);
   if (e != cudaSuccess) return cuda_fail(e, "emb_table_slots");
+  return EMB_OK;
+}
+
+emb_status emb_debug_fail_device_alloc(int64_t after) {
+  g_fail_after.store(after < 0 ? -1 : (long long)after);
+  return EMB_OK;
+}
+
+int64_t emb_debug_live_device_allocs(void) { return (int64_t)g_live_allocs.load(); }
+
+emb_status emb_debug_set_probe_bound(emb_table* table, int64_t bound) {
+  if (!table || bound < 1 || bound > table->st.max_cluster + 1)
+    return fail(EMB_ERR_INVALID_ARG, "probe bound must be in [1, max_cluster + 1]");
+  table->st.probe_bound = bound;
   return EMB_OK;
 }
 

@@ -4,6 +4,7 @@ import ctypes
 
 import numpy as np
 import pytest
+import torch
 
 import oracle
 import workload as W
@@ -98,3 +99,19 @@ def test_master_copy_tables_plan_like_f16_tables():
     with pytest.raises(E.EmbError):
         E.emb_table_plan([12], "f16m", keys[:4] & ((1 << 48) - 1), 16)     # f16 rows need dims % 8 == 0
 
+
+
+def test_failed_create_returns_oom_and_leaves_nothing_allocated():
+    """Fault injection on the host: the table's first device allocation fails;
+    create must return EMB_ERR_OOM (not abort) and hold no device memory.
+    Nothing reaches CUDA, so this runs without a GPU."""
+    keys = torch.tensor([(0 << 48) | 5, (1 << 48) | 7], dtype=torch.int64)
+    live0 = E.emb_debug_live_device_allocs()
+    E.emb_debug_fail_device_alloc(0)
+    try:
+        with pytest.raises(E.EmbError) as ei:
+            E.emb_table_create([8, 8], "f32", keys, capacity=8, stream=0)   # no torch stream on a CPU box
+    finally:
+        E.emb_debug_fail_device_alloc(-1)
+    assert ei.value.name == "EMB_ERR_OOM"
+    assert E.emb_debug_live_device_allocs() == live0

@@ -5,11 +5,20 @@ against the oracle's FTRL, over several steps in a row so that the state
 Gates (tol as for Adagrad; see parity_util for dg, the bound on the float32
 per-key gradient's error, nonzero only for keys whose terms cancel):
   n        |x - r| <= tol * r + 2|g| dg + dg^2                (n' = n + g^2, as Adagrad's acc)
-  z        |x - r| <= tol * max(|r|, |z_old| + |g| + |sigma w_old|) + dg
+  z        |x - r| <= tol * max(|r|, |z_old| + |g| + |sigma w_old|) + dg + ds
            (z' = z + g - sigma w is a sum whose terms can cancel)
-  weight   |x - r| <= tol * max(|r|, |w_old|, |z'| / den) + dg / den,  den = (beta + sqrt(n')) / alpha + lambda2
+  weight   |x - r| <= tol * max(|r|, |w_old|, |z'| / den) + (dg + ds) / den,
+           den = (beta + sqrt(n')) / alpha + lambda2
            (w' = -(z' - sign(z') lambda1) / den: near the threshold |z'| = lambda1 the
            shrunk weight is small, so its error is measured against the unshrunk |z'| / den)
+ds is the conditioning of sigma itself: sigma = (sqrt(n') - sqrt(n)) / alpha is a
+difference of two nearly equal square roots when g^2 << n, so the last bit of
+n' (which follows g's last bit) moves sigma by about u sqrt(n') / alpha, and z
+by that times |w|; both sides evaluate the same float32 formula, so
+  ds = 4 u sqrt(n') |w_old| / alpha + |g| dg' |w_old| / (alpha sqrt(n'))
+bounds the difference that g's own error dg' = DG_ULPS u A_g + u |g| (every
+key, cancelling or not) and the roundings of n' and the square roots can make
+(u = 2^-24).
 """
 import numpy as np
 import pytest
@@ -18,7 +27,7 @@ import torch
 import oracle
 import workload as W
 import sparse_ctr_embedding_gb300 as E
-from parity_util import elem_index, gate, grad_err, report, tol_of
+from parity_util import DG_ULPS, U32, elem_index, gate, grad_err, report, tol_of
 
 pytestmark = pytest.mark.gpu
 
@@ -94,16 +103,20 @@ def _run(cfg, wdtype=None, steps=3):
         w[idx], n[idx], z[idx] = w_r, n_r, z_r
         dg = grad_err(G, Ag)
         absg = np.abs(G)
-        sigma = (np.sqrt(n_r.astype(np.float64)) - np.sqrt(n_old.astype(np.float64))) / ALPHA
-        den = (BETA + np.sqrt(n_r.astype(np.float64))) / ALPHA + L2
+        sn1 = np.sqrt(n_r.astype(np.float64))
+        absw = np.abs(w_old.astype(np.float64))
+        sigma = (sn1 - np.sqrt(n_old.astype(np.float64))) / ALPHA
+        den = (BETA + sn1) / ALPHA + L2
+        dg_all = DG_ULPS * U32 * Ag + U32 * absg             # the gradient's error bound, every key
+        ds = 4 * U32 * sn1 * absw / ALPHA + absg * dg_all * absw / (ALPHA * sn1)
         gate(f"n, step {k + 1}", n_x[idx], n_r, n_r.astype(np.float64) + (2 * absg * dg + dg * dg) / tol, tol)
         gate(f"z, step {k + 1}", z_x[idx], z_r,
              np.maximum(np.abs(z_r.astype(np.float64)),
                         np.abs(z_old.astype(np.float64)) + absg + np.abs(sigma * w_old.astype(np.float64)))
-             + dg / tol, tol)
+             + (dg + ds) / tol, tol)
         gate(f"weights, step {k + 1}", w_x[idx].astype(np.float64), w_r.astype(np.float64),
-             np.maximum(np.maximum(np.abs(w_r.astype(np.float64)), np.abs(w_old.astype(np.float64))),
-                        np.abs(z_r.astype(np.float64)) / den) + dg / den / tol, tol)
+             np.maximum(np.maximum(np.abs(w_r.astype(np.float64)), absw),
+                        np.abs(z_r.astype(np.float64)) / den) + (dg + ds) / den / tol, tol)
         # rows the batch does not hit: bit-identical to the oracle's (unchanged) state
         untouched = np.ones(n_el, bool)
         untouched[idx] = False
