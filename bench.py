@@ -39,6 +39,9 @@ def parse():
     ap.add_argument("--wdtype", default=None, choices=["f32", "f16", "f16m"],
                     help="weight storage instead of the workload's own (f16m: f32 master rows + f16 copy)")
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--fwd", default="fused", choices=["fused", "dedup"],
+                    help="forward: the fused lookup + pooling (default), or the within-batch dedupe forward "
+                         "(pairs sorted first, each unique row read once; the backward then skips its sort)")
     ap.add_argument("--vocab-div", type=int, default=1, help="shrink keys per slot (profiling a small case)")
     ap.add_argument("--batch-div", type=int, default=1, help="shrink the batch (profiling a small case)")
     ap.add_argument("--cpu-samples", type=int, default=2048,
@@ -165,14 +168,16 @@ def max_over_ranks(ws, x: float) -> float:
     return float(t.item())
 
 
-def launches_per_step(max_slot_keys: int, digit_bits: int) -> int:
-    """Kernels this library launches for one recording fwd + one recorded bwd call.
+def launches_per_step(max_slot_keys: int, digit_bits: int, dedup: bool = False) -> int:
+    """Kernels this library launches for one forward (recording, or with dedupe) + one recorded bwd call.
     The backward sorts rows within a slot, so the pass count follows the largest slot."""
     bits = max(1, int(max_slot_keys).bit_length())
     passes = max(1, math.ceil(bits / digit_bits))
-    # placement (3 scan kernels + region setup) + recording fwd; (count + 3 scan + scatter)
-    # per radix pass; reduce; fixup
-    return 5 + passes * 5 + 2
+    # placement (transpose + 3 scan kernels + region setup + tile map); recording fwd, or expand + the
+    # sort + dedupe pooling; (count + 3 scan + scatter) per radix pass; reduce; fixup
+    if dedup:
+        return 6 + 1 + passes * 5 + 1 + 2
+    return 6 + 1 + passes * 5 + 2
 
 
 # ------------------------------------------------------------------ oracle (CPU baseline / reference arm)
@@ -344,9 +349,13 @@ def run_ours(args):
     io_bytes = 8 * nnz + 16 * nnz * p_bar + 4 * cfg.batch * cfg.sum_dims + 8 * (n_bags + 1)
     fwd_bytes = io_bytes + gather_bytes
 
+    fwd = E.emb_lookup_fwd_dedup if args.fwd == "dedup" else E.emb_lookup_fwd_record
+    fwd_name = ("forward with dedupe (expand + sort + dedup_pool_kernel)" if args.fwd == "dedup"
+                else "fwd_pool_kernel")
+
     def step():
         # the forward records each occurrence's resolved row for the backward
-        E.emb_lookup_fwd_record(tbl, offsets, qkeys, cfg.pool, wsb, out=out)
+        fwd(tbl, offsets, qkeys, cfg.pool, wsb, out=out)
         E.emb_bwd_adagrad_recorded(tbl, n_bags, nnz, cfg.pool, grad, cfg.lr, cfg.eps, wsb)
 
     step()
@@ -365,7 +374,7 @@ def run_ours(args):
     bwd_bytes = 4 * nnz + 8 * (n_bags + 1) + 4 * cfg.batch * cfg.sum_dims + rmw_bytes
     # algorithmic bytes per launch of each kernel (sort and partial sums are overhead)
     kernel_bytes = {
-        "fwd_pool_kernel": fwd_bytes,
+        fwd_name: fwd_bytes,
         "segreduce_update_kernel": 4 * cfg.batch * cfg.sum_dims + rmw_bytes,
     }
     flags = E.emb_check_device_flag(tbl)
@@ -385,7 +394,7 @@ def run_ours(args):
     torch.cuda.synchronize()
     for k in range(K):
         ev[k][0].record(stream)
-        E.emb_lookup_fwd_record(tbl, offsets, qkeys, cfg.pool, wsb, out=out)
+        fwd(tbl, offsets, qkeys, cfg.pool, wsb, out=out)
         ev[k][1].record(stream)
         E.emb_bwd_phase_events(tbl, ev[k][2:-1])
         E.emb_bwd_adagrad_recorded(tbl, n_bags, nnz, cfg.pool, grad, cfg.lr, cfg.eps, wsb)
@@ -402,7 +411,7 @@ def run_ours(args):
     total_ms = max_over_ranks(ws, total_ms)
     ms_step = total_ms / K
     flags |= E.emb_check_device_flag(tbl)
-    kernel_ms = {"fwd_pool_kernel": fwd_ms,
+    kernel_ms = {fwd_name: fwd_ms,
                  "radix sort (count + scan + scatter kernels)": phase_ms["sort"],
                  "segreduce_update_kernel": phase_ms["reduce"], "fixup_kernel": phase_ms["fixup"]}
 
@@ -491,7 +500,7 @@ def run_ours(args):
         "fwd_roofline": {"achieved": fwd_gbs, "frac": fwd_gbs / peak, "algorithmic_bytes": fwd_bytes},
         "bwd_roofline": {"achieved": bwd_gbs, "frac": bwd_gbs / peak, "algorithmic_bytes": bwd_bytes},
         "cpu_baseline": cpu, "e2e": e2e,
-        "gpu_launches": K * launches_per_step(st["max_slot_keys"], E.EMB_SORT_DIGIT_BITS),
+        "gpu_launches": K * launches_per_step(st["max_slot_keys"], E.EMB_SORT_DIGIT_BITS, args.fwd == "dedup"),
         "clocks": clk, "device_flags": flags,
         "setup_s": {"generate": t_gen, "table_create": t_create, "table_create_device": t_create_dev},
     }

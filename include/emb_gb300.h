@@ -345,6 +345,23 @@ EMB_API emb_status emb_bwd_ftrl_recorded(emb_table* table, int64_t n_bags, int64
                                          size_t ws_bytes, void* stream);
 
 /*
+ * emb_lookup_fwd_dedup -- the forward with a within-batch dedupe (Tencent PCG
+ * talk, "各阶段优化详细介绍": a group's keys are deduplicated before their
+ * rows are moved): every occurrence is resolved and its (row, bag) pair
+ * placed and sorted by row, as the backward does; each unique row is then
+ * read from the table once and added into every bag that holds it.  The
+ * sorted pairs stay in the workspace, so emb_bwd_adagrad_recorded /
+ * emb_bwd_ftrl_recorded called next skip their sort.  Arguments, workspace
+ * and errors as emb_lookup_fwd_record.  The pooled adds of a bag come from
+ * several warps, as float32 atomics, so `out` agrees with emb_lookup_fwd to
+ * within float32 rounding of the sum but is not bitwise reproducible (the
+ * update that follows is, as after emb_lookup_fwd_record).
+ */
+EMB_API emb_status emb_lookup_fwd_dedup(emb_table* table, const int64_t* offsets_d, int64_t n_bags,
+                                        const int64_t* keys_d, int64_t nnz, emb_pool pool, float* out_d,
+                                        void* workspace_d, size_t ws_bytes, void* stream);
+
+/*
  * emb_bwd_unique_keys -- the deduplicated key set of the last emb_bwd_adagrad
  * that used this workspace (Tencent PCG talk, "各阶段优化详细介绍": the
  * deduplicated keys a group uses are what the pass moves between the GPU table

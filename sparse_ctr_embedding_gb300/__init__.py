@@ -21,7 +21,7 @@ from .build import HEADER, LIB_PATH, build
 __all__ = [
     "EmbError", "LibraryNotBuilt", "Table", "lib", "declared_symbols",
     "emb_table_create", "emb_table_create_device", "emb_table_destroy", "emb_table_get_stats", "emb_table_plan",
-    "emb_lookup_fwd", "emb_lookup_fwd_record", "emb_bwd_adagrad_recorded", "emb_bwd_workspace_size", "emb_bwd_adagrad", "emb_bwd_adagrad_noalloc",
+    "emb_lookup_fwd", "emb_lookup_fwd_record", "emb_lookup_fwd_dedup", "emb_bwd_adagrad_recorded", "emb_bwd_workspace_size", "emb_bwd_adagrad", "emb_bwd_adagrad_noalloc",
     "emb_bwd_ftrl", "emb_bwd_ftrl_recorded", "emb_table_export_z", "emb_table_import_z",
     "emb_debug_fail_device_alloc", "emb_debug_live_device_allocs", "emb_debug_set_probe_bound", "Pipeline",
     "emb_bwd_unique_keys", "emb_bwd_phase_events", "EMB_NOALLOC_SCRATCH_BYTES", "EMB_SORT_DIGIT_BITS", "BWD_PHASES",
@@ -103,6 +103,7 @@ def lib():
             "emb_bwd_unique_keys": [_vp, _vp, ctypes.c_size_t, _vp, _vp, _vp],
             "emb_bwd_phase_events": [_vp, ctypes.POINTER(_vp), ctypes.c_int],
             "emb_lookup_fwd_record": [_vp, _vp, _i64, _vp, _i64, ctypes.c_int, _vp, _vp, ctypes.c_size_t, _vp],
+            "emb_lookup_fwd_dedup": [_vp, _vp, _i64, _vp, _i64, ctypes.c_int, _vp, _vp, ctypes.c_size_t, _vp],
             "emb_bwd_adagrad_recorded": [_vp, _i64, _i64, ctypes.c_int, _vp, ctypes.c_float, ctypes.c_float, _vp,
                                          ctypes.c_size_t, _vp],
             "emb_bwd_adagrad_noalloc": [_vp, _vp, _i64, _vp, _i64, ctypes.c_int, _vp, ctypes.c_float,
@@ -304,6 +305,20 @@ def emb_lookup_fwd_record(table: Table, offsets: torch.Tensor, keys: torch.Tenso
                                        _cuda(keys, torch.int64, "keys"), keys.numel(), _POOL[pool],
                                        _cuda(out, torch.float32, "out"), _cuda(workspace, None, "workspace"),
                                        workspace.numel() * workspace.element_size(), _stream(stream)))
+    return out
+
+
+def emb_lookup_fwd_dedup(table: Table, offsets: torch.Tensor, keys: torch.Tensor, pool: str, workspace: torch.Tensor,
+                         out: Optional[torch.Tensor] = None, stream=None) -> torch.Tensor:
+    """The forward with a within-batch dedupe: pairs placed and sorted by row,
+    each unique row read once; the recorded backward that follows skips its sort."""
+    n_bags = offsets.numel() - 1
+    if out is None:
+        out = torch.empty((n_bags // table.n_slots, sum(table.dims)), dtype=torch.float32, device=offsets.device)
+    _check(lib().emb_lookup_fwd_dedup(table.handle, _cuda(offsets, torch.int64, "offsets"), n_bags,
+                                      _cuda(keys, torch.int64, "keys"), keys.numel(), _POOL[pool],
+                                      _cuda(out, torch.float32, "out"), _cuda(workspace, None, "workspace"),
+                                      workspace.numel() * workspace.element_size(), _stream(stream)))
     return out
 
 

@@ -1384,6 +1384,34 @@ static emb_status launch_placement(const emb_table* t, const int64_t* offsets_d,
   return EMB_OK;
 }
 
+// The stable sort of the placed (row, bag) pairs by row, region by region.
+// Returns the buffers holding the sorted pairs (A or B by the pass count).
+static emb_status sort_placed_pairs(const emb_table* table, int64_t n_bags, unsigned n, char* ws, const WsLayout& L,
+                                    cudaStream_t st, unsigned** k_sorted, unsigned** v_sorted) {
+  const int passes = sort_passes(table);
+  unsigned* counts = (unsigned*)(ws + L.counts);
+  unsigned* partials = (unsigned*)(ws + L.partials);
+  const size_t smem = scatter_smem();
+  EMB_CUDA(cudaFuncSetAttribute(radix_scatter_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem));
+  unsigned *ki = (unsigned*)(ws + L.kA), *vi = (unsigned*)(ws + L.vA);
+  unsigned *ko = (unsigned*)(ws + L.kB), *vo = (unsigned*)(ws + L.vB);
+  const SortSeg* sg = (const SortSeg*)(ws + L.sseg);
+  const unsigned* treg = (const unsigned*)(ws + L.treg);
+  for (int p = 0; p < passes; ++p) {
+    const int shift = p * kRadixBits;
+    radix_count_kernel<<<L.n_tiles_sort, kSortThreads, 0, st>>>(ki, sg, L.n_regions, shift, counts, treg);
+    EMB_CUDA(launch_scan(counts, counts, (size_t)kDigits * L.n_tiles_sort, partials, st));
+    radix_scatter_kernel<<<L.n_tiles_sort, kSortThreads, smem, st>>>(ki, vi, ko, vo, shift, counts, sg, L.n_regions,
+                                                                     (unsigned)table->st.n_keys, (unsigned)n_bags, treg);
+    EMB_CUDA(cudaGetLastError());
+    std::swap(ki, ko);
+    std::swap(vi, vo);
+  }
+  *k_sorted = ki;
+  *v_sorted = vi;
+  return EMB_OK;
+}
+
 // The optimizer of one backward call.
 struct BwdOpt {
   bool ftrl;
@@ -1392,10 +1420,11 @@ struct BwdOpt {
 };
 
 // The backward.  With `recorded`, the (row, bag) pairs, 1/L and the header were
-// written by emb_lookup_fwd_record and the expand phase is skipped.
+// written by emb_lookup_fwd_record (or emb_lookup_fwd_dedup, which also sorted
+// them: `presorted`) and those phases are skipped.
 static emb_status run_bwd(emb_table* table, const int64_t* offsets_d, int64_t n_bags, const int64_t* keys_d,
                           int64_t nnz, emb_pool pool, const float* grad_out_d, const BwdOpt& opt, char* ws,
-                          const WsLayout& L, cudaStream_t st, bool recorded = false) {
+                          const WsLayout& L, cudaStream_t st, bool recorded = false, bool presorted = false) {
   const unsigned n = (unsigned)nnz;
   // grad_out rows are addressed as 32-bit float4 indices
   if ((unsigned long long)(n_bags / table->st.n_slots) * (unsigned long long)table->st.sum_dims >= (1ULL << 34))
@@ -1426,22 +1455,15 @@ static emb_status run_bwd(emb_table* table, const int64_t* offsets_d, int64_t n_
     return EMB_OK;
   }
 
-  unsigned* counts = (unsigned*)(ws + L.counts);
-  unsigned* partials = (unsigned*)(ws + L.partials);
-  const size_t smem = scatter_smem();
-  EMB_CUDA(cudaFuncSetAttribute(radix_scatter_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem));
-  unsigned *ki = kA, *vi = vA, *ko = kB, *vo = vB;
-  const SortSeg* sg = (const SortSeg*)(ws + L.sseg);
-  const unsigned* treg = (const unsigned*)(ws + L.treg);
-  for (int p = 0; p < passes; ++p) {
-    const int shift = p * kRadixBits;
-    radix_count_kernel<<<L.n_tiles_sort, kSortThreads, 0, st>>>(ki, sg, L.n_regions, shift, counts, treg);
-    EMB_CUDA(launch_scan(counts, counts, (size_t)kDigits * L.n_tiles_sort, partials, st));
-    radix_scatter_kernel<<<L.n_tiles_sort, kSortThreads, smem, st>>>(ki, vi, ko, vo, shift, counts, sg, L.n_regions,
-                                                                     (unsigned)table->st.n_keys, (unsigned)n_bags, treg);
-    EMB_CUDA(cudaGetLastError());
-    std::swap(ki, ko);
-    std::swap(vi, vo);
+  unsigned *ki = kA, *vi = vA;
+  if (presorted) {
+    if (passes & 1) {
+      ki = kB;
+      vi = vB;
+    }
+  } else {
+    emb_status rc = sort_placed_pairs(table, n_bags, n, ws, L, st, &ki, &vi);
+    if (rc != EMB_OK) return rc;
   }
   mark_phase(table, 1, st);
   // ki/vi hold the sorted pairs
@@ -1456,6 +1478,86 @@ static emb_status run_bwd(emb_table* table, const int64_t* offsets_d, int64_t n_
              : dispatch_reduce<float>(table, ki, vi, scale, mean, grad_out_d, n, nb, L, ws, opt.ada, st);
   if (e != cudaSuccess) return cuda_fail(e, "segmented reduce launch");
   return EMB_OK;
+}
+
+// ------------------------------------------------------------------ forward with a within-batch dedupe
+//
+// The Tencent PCG talk ("各阶段优化详细介绍") deduplicates the keys of a group
+// before their rows are moved.  Here the dedupe is the backward's own work
+// done first: every occurrence resolved and placed, the pairs sorted by row;
+// then each unique row is read from the table once, into registers, and added
+// into every bag that holds it.  The sorted pairs stay in the workspace, so
+// the recorded backward that follows skips its sort.  A pooled row receives
+// adds from many warps, so they are float32 atomics: the output agrees with
+// emb_lookup_fwd within rounding but is not bitwise reproducible.
+constexpr int kDedupChunk = 64;  // sorted positions per lane group
+
+template <typename TW, int NCB>
+__global__ void __launch_bounds__(256) dedup_pool_kernel(TableView t, const unsigned* __restrict__ K,
+                                                         const unsigned* __restrict__ V,
+                                                         const float* __restrict__ scale, int mean, unsigned n,
+                                                         unsigned n_bags, float* __restrict__ out, int G) {
+  const int lane = threadIdx.x & 31;
+  const int P = 32 / G;
+  const int sub = lane / G, li = lane % G;
+  const unsigned gid = ((blockIdx.x * blockDim.x + threadIdx.x) >> 5) * P + sub;
+  const unsigned ngroups = ((gridDim.x * blockDim.x) >> 5) * P;
+  const unsigned S = (unsigned)t.n_slots, miss = t.n_rows;
+  const TW* W = static_cast<const TW*>(t.W);
+  for (unsigned long long c0 = (unsigned long long)gid * kDedupChunk; c0 < n;
+       c0 += (unsigned long long)ngroups * kDedupChunk) {
+    const unsigned c1 = (unsigned)min(c0 + kDedupChunk, (unsigned long long)n);
+    unsigned cur = kNoRow;
+    RowGeo g{0, 0, 0, false};
+    float w[NCB][4];
+    for (unsigned i = (unsigned)c0; i < c1; ++i) {
+      const unsigned row = K[i], bag = V[i];
+      if (row >= miss || bag >= n_bags) continue;
+      if (row != cur) {  // a new run: its row is read from the table once
+        cur = row;
+        g = geo_from_slot(t, row, (int)(bag % S));
+#pragma unroll
+        for (int cc = 0; cc < NCB; ++cc) {
+          const int ce = (cc * G + li) * 4;
+          if (g.ok && ce < g.D) {
+            ldw4(W + g.e0 + ce, w[cc]);
+          } else {
+            w[cc][0] = w[cc][1] = w[cc][2] = w[cc][3] = 0.f;
+          }
+        }
+      }
+      if (!g.ok) continue;
+      const float sc = mean ? scale[bag] : 1.f;
+      float* o = out + (size_t)(bag / S) * (unsigned)t.sum_dims + (unsigned)g.col;
+#pragma unroll
+      for (int cc = 0; cc < NCB; ++cc) {
+        const int ce = (cc * G + li) * 4;
+        if (ce < g.D)
+          atomicAdd(reinterpret_cast<float4*>(o + ce),
+                    make_float4(w[cc][0] * sc, w[cc][1] * sc, w[cc][2] * sc, w[cc][3] * sc));
+      }
+    }
+  }
+}
+
+template <typename TW>
+static cudaError_t launch_dedup_pool(const emb_table* t, const unsigned* K, const unsigned* V, const float* scale,
+                                     int mean, unsigned n, unsigned n_bags, float* out, cudaStream_t st) {
+  const int vecs = (t->st.max_dim + 3) / 4;  // 4-float column vectors of the widest row
+  int G = 1;
+  while (G < vecs && G < 32) G <<= 1;
+  const int ncb = (vecs + G - 1) / G;
+  const unsigned groups = (n + kDedupChunk - 1) / kDedupChunk;
+  const long long blocks =
+      std::max(1LL, std::min<long long>(((long long)groups * G + 255) / 256, (long long)sm_count() * 8));
+  TableView v = t->fwd_view();  // master-copy tables: the f16 copy, as the forward reads
+  if (ncb <= 1)
+    dedup_pool_kernel<TW, 1><<<(int)blocks, 256, 0, st>>>(v, K, V, scale, mean, n, n_bags, out, G);
+  else if (ncb <= 2)
+    dedup_pool_kernel<TW, 2><<<(int)blocks, 256, 0, st>>>(v, K, V, scale, mean, n, n_bags, out, G);
+  else
+    dedup_pool_kernel<TW, 4><<<(int)blocks, 256, 0, st>>>(v, K, V, scale, mean, n, n_bags, out, G);
+  return cudaGetLastError();
 }
 
 // Scratch for emb_bwd_adagrad_noalloc, for callers that cannot allocate
@@ -1575,6 +1677,7 @@ emb_status emb_lookup_fwd_record(emb_table* table, const int64_t* offsets_d, int
   table->rec_nnz = nnz;
   table->rec_bags = n_bags;
   table->rec_pool = (int)pool;
+  table->rec_sorted = false;
   return EMB_OK;
 }
 
@@ -1592,7 +1695,7 @@ static emb_status bwd_recorded(emb_table* table, int64_t n_bags, int64_t nnz, em
   const WsLayout L = ws_layout(table, n_bags, nnz);
   if (ws_bytes < L.total) return fail(EMB_ERR_WORKSPACE, "workspace missing or too small");
   return run_bwd(table, nullptr, n_bags, nullptr, nnz, pool, grad_out_d, opt, (char*)workspace_d, L,
-                 (cudaStream_t)stream, true);
+                 (cudaStream_t)stream, true, table->rec_sorted);
 }
 
 // The backward with a caller workspace and either optimizer.
@@ -1617,6 +1720,49 @@ static emb_status ftrl_opt(const emb_ftrl_params* p, BwdOpt* o) {
   if (!(p->alpha > 0.f) || !(p->beta >= 0.f) || !(p->lambda1 >= 0.f) || !(p->lambda2 >= 0.f))
     return fail(EMB_ERR_INVALID_ARG, "FTRL needs alpha > 0 and beta, lambda1, lambda2 >= 0");
   *o = BwdOpt{true, {}, {p->alpha, p->beta, p->lambda1, p->lambda2}};
+  return EMB_OK;
+}
+
+emb_status emb_lookup_fwd_dedup(emb_table* table, const int64_t* offsets_d, int64_t n_bags, const int64_t* keys_d,
+                                int64_t nnz, emb_pool pool, float* out_d, void* workspace_d, size_t ws_bytes,
+                                void* stream) {
+  emb_status rc = check_batch(table, offsets_d, n_bags, keys_d, nnz, pool);
+  if (rc != EMB_OK) return rc;
+  if (n_bags > 0 && !out_d) return fail(EMB_ERR_INVALID_ARG, "out is NULL");
+  if (((uintptr_t)out_d & 15) != 0) return fail(EMB_ERR_INVALID_ARG, "out must be 16-byte aligned");
+  const WsLayout L = ws_layout(table, n_bags, nnz);
+  if (!workspace_d || ws_bytes < L.total) return fail(EMB_ERR_WORKSPACE, "workspace missing or too small");
+  if (((uintptr_t)workspace_d & 255) != 0) return fail(EMB_ERR_WORKSPACE, "workspace must be 256-byte aligned");
+  cudaStream_t st = (cudaStream_t)stream;
+  char* ws = (char*)workspace_d;
+  const int mean = pool == EMB_POOL_MEAN;
+  if ((rc = launch_placement(table, offsets_d, n_bags, nnz, ws, L, st)) != EMB_OK) return rc;
+  unsigned* kA = (unsigned*)(ws + L.kA);
+  unsigned* vA = (unsigned*)(ws + L.vA);
+  float* scale = (float*)(ws + L.scale);
+  if (n_bags > 0) {
+    const long long blocks = std::min<long long>((n_bags * 32 + 255) / 256, resident_blocks(256));
+    expand_kernel<<<(int)std::max(1LL, blocks), 256, 0, st>>>(table->fwd_view(), (const long long*)offsets_d,
+                                                              n_bags, (const long long*)keys_d, nnz, mean,
+                                                              (const unsigned*)(ws + L.dest), kA, vA, scale);
+    EMB_CUDA(cudaGetLastError());
+    EMB_CUDA(cudaMemsetAsync(out_d, 0, (size_t)(n_bags / table->st.n_slots) * (size_t)table->st.sum_dims * 4, st));
+  }
+  if (nnz > 0) {
+    unsigned *ki, *vi;
+    if ((rc = sort_placed_pairs(table, n_bags, (unsigned)nnz, ws, L, st, &ki, &vi)) != EMB_OK) return rc;
+    cudaError_t e = table->fwd_half()
+                        ? launch_dedup_pool<__half>(table, ki, vi, scale, mean, (unsigned)nnz, (unsigned)n_bags,
+                                                    out_d, st)
+                        : launch_dedup_pool<float>(table, ki, vi, scale, mean, (unsigned)nnz, (unsigned)n_bags,
+                                                   out_d, st);
+    if (e != cudaSuccess) return cuda_fail(e, "dedup_pool_kernel launch");
+  }
+  table->rec_ws = workspace_d;
+  table->rec_nnz = nnz;
+  table->rec_bags = n_bags;
+  table->rec_pool = (int)pool;
+  table->rec_sorted = true;
   return EMB_OK;
 }
 

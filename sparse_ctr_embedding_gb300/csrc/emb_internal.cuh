@@ -158,6 +158,7 @@ struct emb_table {
   const void* rec_ws = nullptr;
   long long rec_nnz = -1, rec_bags = -1;
   int rec_pool = -1;
+  bool rec_sorted = false;  // the recording forward also sorted the pairs (emb_lookup_fwd_dedup)
 
   emb::TableView view() const {
     emb::TableView v;

@@ -30,9 +30,11 @@ def test_fingerprint_is_stable():
 
 
 def test_launches_per_step_follow_the_digit_width():
-    # placement (4) + recording forward, 5 launches per radix pass, reduce, fixup;
+    # placement (6) + recording forward, 5 launches per radix pass, reduce, fixup;
     # the backward sorts rows within a slot: the largest slot's key count sets the passes
-    assert bench.launches_per_step(1_562_500, E.EMB_SORT_DIGIT_BITS) == 5 + 3 * 5 + 2     # 21 bits, 3 passes
-    assert bench.launches_per_step(16_383, E.EMB_SORT_DIGIT_BITS) == 5 + 2 * 5 + 2        # 14 bits, 2 passes
-    assert bench.launches_per_step(16_384, E.EMB_SORT_DIGIT_BITS) == 5 + 3 * 5 + 2        # 15 bits, 3 passes
-    assert bench.launches_per_step(100, 7) == 5 + 1 * 5 + 2
+    assert bench.launches_per_step(1_562_500, E.EMB_SORT_DIGIT_BITS) == 7 + 3 * 5 + 2     # 21 bits, 3 passes
+    assert bench.launches_per_step(16_383, E.EMB_SORT_DIGIT_BITS) == 7 + 2 * 5 + 2        # 14 bits, 2 passes
+    assert bench.launches_per_step(16_384, E.EMB_SORT_DIGIT_BITS) == 7 + 3 * 5 + 2        # 15 bits, 3 passes
+    assert bench.launches_per_step(100, 7) == 7 + 1 * 5 + 2
+    # the dedupe forward: placement, expand, the sort, dedupe pooling; the backward skips its sort
+    assert bench.launches_per_step(1_562_500, E.EMB_SORT_DIGIT_BITS, dedup=True) == 7 + 3 * 5 + 1 + 2
