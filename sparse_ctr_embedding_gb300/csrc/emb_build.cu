@@ -254,11 +254,14 @@ struct RunSmem {
   unsigned occ[(CAP + 31) / 32];
 };
 
+// The leader adds the run's probe lengths to *sum and raises *mx (its own
+// running totals: one atomic per warp or block at the end, not per run).
 template <int CAP>
 __device__ void replay_run(RunSmem<CAP>& sm, const long long* __restrict__ keys, const unsigned* __restrict__ RH,
                            const unsigned* __restrict__ RI, const long long* __restrict__ P, unsigned a, unsigned m,
                            unsigned long long mask, unsigned long long r0, unsigned* __restrict__ fin,
-                           BuildInfo* info, int tid, int nthreads, bool leader) {
+                           BuildInfo* info, int tid, int nthreads, bool leader, unsigned long long* sum,
+                           unsigned long long* mx) {
   const long long pa = P[a];
   for (unsigned t = tid; t < m; t += nthreads) {
     sm.hr[t] = (unsigned)((long long)RH[a + t] - pa);
@@ -283,7 +286,6 @@ __device__ void replay_run(RunSmem<CAP>& sm, const long long* __restrict__ keys,
   if (nthreads == 32) __syncwarp(); else __syncthreads();
   if (leader) {
     const unsigned nw = (m + 31) / 32;
-    unsigned long long sum = 0, mx = 0;
     for (unsigned q = 0; q < m; ++q) {
       const unsigned t = sm.order[q];
       const unsigned h = sm.hr[t];
@@ -298,11 +300,9 @@ __device__ void replay_run(RunSmem<CAP>& sm, const long long* __restrict__ keys,
       sm.occ[w] |= 1u << (pos & 31);
       fin[sm.idx[t]] = (unsigned)(((unsigned long long)(pa + pos) + r0) & mask);
       const unsigned long long len = (unsigned long long)(pos - h + 1);
-      sum += len;
-      mx = max(mx, len);
+      *sum += len;
+      *mx = max(*mx, len);
     }
-    atomicAdd(&info->sum_probe, sum);
-    atomicMax(&info->max_probe, mx);
   }
 }
 
@@ -318,10 +318,11 @@ __global__ void __launch_bounds__(kRunWarps * 32) run_warp_kernel(
   const unsigned R = *n_runs_p;
   const unsigned long long r0 = cinfo->r0;
   const unsigned nwarps = gridDim.x * kRunWarps;
+  unsigned long long sum = 0, mx = 0, mrun = 0;
   for (unsigned k = blockIdx.x * kRunWarps + w; k < R; k += nwarps) {
     const unsigned a = RS[k], b = k + 1 < R ? RS[k + 1] : n;
     const unsigned m = b - a;
-    if (lane == 0) atomicMax(&info->max_run, (unsigned long long)m);
+    mrun = max(mrun, (unsigned long long)m);
     if (m > kWarpRun) {
       if (lane == 0) {
         if (m > kMaxRun) atomicOr(&info->too_long, 1ULL);
@@ -329,8 +330,13 @@ __global__ void __launch_bounds__(kRunWarps * 32) run_warp_kernel(
       }
       continue;
     }
-    replay_run<kWarpRun>(sm[w], keys, RH, RI, P, a, m, mask, r0, fin, info, lane, 32, lane == 0);
+    replay_run<kWarpRun>(sm[w], keys, RH, RI, P, a, m, mask, r0, fin, info, lane, 32, lane == 0, &sum, &mx);
     __syncwarp();
+  }
+  if (lane == 0) {
+    if (sum) atomicAdd(&info->sum_probe, sum);
+    if (mx) atomicMax(&info->max_probe, mx);
+    if (mrun) atomicMax(&info->max_run, mrun);
   }
 }
 
@@ -344,12 +350,17 @@ __global__ void __launch_bounds__(256) run_block_kernel(
   const unsigned R = *n_runs_p;
   const unsigned L = (unsigned)cinfo->n_long;
   const unsigned long long r0 = cinfo->r0;
+  unsigned long long sum = 0, mx = 0;
   for (unsigned q = blockIdx.x; q < L; q += gridDim.x) {
     const unsigned k = long_list[q];
     const unsigned a = RS[k], b = k + 1 < R ? RS[k + 1] : n;
     replay_run<kMaxRun>(sm, keys, RH, RI, P, a, b - a, mask, r0, fin, info, threadIdx.x, blockDim.x,
-                        threadIdx.x == 0);
+                        threadIdx.x == 0, &sum, &mx);
     __syncthreads();
+  }
+  if (threadIdx.x == 0) {
+    if (sum) atomicAdd(&info->sum_probe, sum);
+    if (mx) atomicMax(&info->max_probe, mx);
   }
 }
 

@@ -123,6 +123,9 @@ def _run(cfg, wdtype=None, steps=3):
         assert np.array_equal(w_x[untouched].view(np.uint8), w[untouched].astype(w_x.dtype).view(np.uint8))
         assert np.array_equal(n_x[untouched], n[untouched]) and np.array_equal(z_x[untouched], z[untouched])
         zeros += int((w_x[idx] == 0).sum())
+        # the next step starts both sides from the GPU's state: each step is checked
+        # from identical inputs (independent roundings would otherwise compound)
+        w[idx], n[idx], z[idx] = w_x[idx], n_x[idx], z_x[idx]
         report(f"ftrl/{cfg.name}/{wd}/step{k + 1}", n_elems=int(idx.size), zero_weights=int((w_x[idx] == 0).sum()),
                oracle_zero_weights=int((w_r == 0).sum()))
     assert zeros > 0                                   # lambda1 made weights exactly 0 (sparsity)
