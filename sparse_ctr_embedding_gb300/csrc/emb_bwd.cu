@@ -248,6 +248,7 @@ __global__ void __launch_bounds__(kSortThreads) radix_count_kernel(const unsigne
                                                                    unsigned* __restrict__ counts,
                                                                    const unsigned* __restrict__ tile_reg) {
   __shared__ unsigned cnt[kSortWarps][kDigits];
+  __shared__ unsigned tkeys[kSortTile + kSortTile / 16];
   __shared__ unsigned reg;
   const int w = threadIdx.x >> 5;
   const unsigned tile = blockIdx.x;
@@ -262,18 +263,22 @@ __global__ void __launch_bounds__(kSortThreads) radix_count_kernel(const unsigne
   const SortSeg g = sg[r];
   const unsigned nt = sg[r + 1].tile0 - g.tile0, lt = tile - g.tile0;
   const unsigned lo = g.lo + lt * kSortTile, hi = min(lo + kSortTile, g.hi);
+  // the tile is read coalesced into shared memory (regions start anywhere, so
+  // a thread's 16 consecutive keys are rarely 16-byte aligned in global
+  // memory), then each thread takes its 16 consecutive keys from there;
+  // element e sits at e + e / 16 (conflict-free both ways)
+#pragma unroll
+  for (int j = 0; j < kSortItems; ++j) {
+    const unsigned e = j * kSortThreads + threadIdx.x;
+    tkeys[e + (e >> 4)] = lo + e < hi ? keys[lo + e] : 0u;
+  }
+  __syncthreads();
   const unsigned base = lo + threadIdx.x * kSortItems;
   unsigned k[kSortItems];
-  if ((lo & 3u) == 0 && base + kSortItems <= hi) {
-    const uint4* p = reinterpret_cast<const uint4*>(keys + base);
 #pragma unroll
-    for (int q = 0; q < kSortItems / 4; ++q) {
-      const uint4 x = __ldg(p + q);
-      k[4 * q] = x.x; k[4 * q + 1] = x.y; k[4 * q + 2] = x.z; k[4 * q + 3] = x.w;
-    }
-  } else {
-#pragma unroll
-    for (int j = 0; j < kSortItems; ++j) k[j] = base + j < hi ? keys[base + j] : 0u;
+  for (int j = 0; j < kSortItems; ++j) {
+    const unsigned e = threadIdx.x * kSortItems + j;
+    k[j] = tkeys[e + (e >> 4)];
   }
   const int m = base >= hi ? 0 : (int)min((unsigned)kSortItems, hi - base);
   unsigned cur = 0, run = 0;

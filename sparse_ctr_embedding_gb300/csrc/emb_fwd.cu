@@ -105,13 +105,30 @@ __global__ void __launch_bounds__(256, 8) fwd_pool_kernel(TableView t, const lon
   // taken in order from a counter (balances warps over bags of very
   // different lengths)
   long long stat = ((blockIdx.x * (long long)blockDim.x + threadIdx.x) >> 5) * BPW + team;
+  // CSR offsets (and, recording, the pairs' slot-major positions) of a team's
+  // batch of bags, staged in shared memory with one load per lane: each bag
+  // then starts its key -> slot -> row chain without two dependent global reads
+  __shared__ long long s_off[8][BPW][kBagBatch + 1];
+  __shared__ unsigned s_dst[8][BPW][kBagBatch];
+  const int wib = threadIdx.x >> 5;
   for (;;) {
     long long b_lo, b_hi;
     if (rec.work) {
       unsigned long long v = 0;
       if (tl == 0) v = atomicAdd(rec.work, (unsigned long long)kBagBatch);
-      b_lo = (long long)__shfl_sync(tmask, v, 0, TEAM);
+      b_lo = (long long)__shfl_sync(tmask, v, 0, TEAM);  // also: the team is done with the last batch
       b_hi = min(b_lo + kBagBatch, n_bags);
+      if (b_lo < n_bags) {
+        const int nb = (int)(b_hi - b_lo);
+        for (int j = tl; j <= nb; j += TEAM) s_off[wib][team][j] = offsets[b_lo + j];
+        if (kRecord)
+          for (int j = tl; j < nb; j += TEAM) {
+            const unsigned bj = (unsigned)(b_lo + j);
+            s_dst[wib][team][j] = rec.dest[(unsigned long long)(bj % (unsigned)t.n_slots) * rec.B +
+                                           bj / (unsigned)t.n_slots];
+          }
+      }
+      __syncwarp(tmask);
     } else {
       b_lo = stat;
       b_hi = stat + 1;
@@ -138,14 +155,24 @@ __global__ void __launch_bounds__(256, 8) fwd_pool_kernel(TableView t, const lon
     const int P = TEAM / G;                           // keys pooled side by side
     const int sub = tl / G, li = tl % G;
 
-    long long start = offsets[bag], end = offsets[bag + 1];
+    long long start, end;
+    if (rec.work) {
+      start = s_off[wib][team][bag - b_lo];
+      end = s_off[wib][team][bag - b_lo + 1];
+    } else {
+      start = offsets[bag];
+      end = offsets[bag + 1];
+    }
     if (start < 0 || end > nnz || end < start || (bag == 0 && start != 0) || (bag == n_bags - 1 && end != nnz)) {
       if (tl == 0) atomicOr(t.flags, EMB_FLAG_BAD_OFFSETS);
       start = min(max(start, 0LL), nnz);
       end = min(max(end, start), nnz);
     }
     // where this bag's pairs go (inside [0, nnz) unless the offsets are malformed)
-    const long long d0 = kRecord ? (long long)rec.dest[(unsigned long long)s * rec.B + (unsigned long long)b] - start : 0;
+    const long long d0 =
+        kRecord ? (long long)(rec.work ? s_dst[wib][team][bag - b_lo]
+                                       : rec.dest[(unsigned long long)s * rec.B + (unsigned long long)b]) - start
+                : 0;
     float acc[NCB][VEC];
 #pragma unroll
     for (int c = 0; c < NCB; ++c)
