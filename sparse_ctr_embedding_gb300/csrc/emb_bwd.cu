@@ -15,7 +15,8 @@
 //               memory so every digit run is written contiguously).
 //               Rows are numbered slot-major, so the sorted order walks one
 //               feature slot (one column block of grad_out) at a time.
-//  3. reduce    the sorted positions are cut into chunks of kChunk; one warp
+//  3. reduce    the sorted positions are cut into sub-chunks (256 positions,
+//               fewer for small batches); one warp
 //               per chunk.  Every run of equal rows inside a chunk ("piece")
 //               is summed in float32 with TwoSum compensation, in sorted
 //               order (so in occurrence order: the sort is stable), by a
@@ -50,7 +51,8 @@ cudaError_t launch_forward(const emb_table* t, const long long* offsets, long lo
                            long long nnz, int mean, float* out, unsigned* K, unsigned* V, float* scale,
                            const unsigned* dest, unsigned long long* work, cudaStream_t st);
 
-constexpr int kChunk = 256;                      // sorted positions per reduce sub-chunk
+constexpr int kChunk = 256;                      // sorted positions per reduce sub-chunk (large batches)
+constexpr int kMinChunk = 32;                    // the shortest sub-chunk (small batches)
 constexpr int kSortWarps = 8;
 constexpr int kSortThreads = kSortWarps * 32;
 constexpr int kSortItems = 16;                   // keys per lane per tile
@@ -89,7 +91,7 @@ static size_t align_up(size_t x) { return (x + 255) & ~(size_t)255; }
 
 struct WsLayout {
   size_t hdr, kA, kB, vA, vB, scale, dest, sseg, treg, counts, partials, partA, partB, arow, zero, work, fwork, uniq, total;
-  unsigned n_tiles_sort, n_regions, n_chunks, n_scan_partials;
+  unsigned n_tiles_sort, n_regions, n_chunks, chunk, n_scan_partials;
   int max_dim;
 };
 
@@ -101,7 +103,12 @@ static WsLayout ws_layout(const emb_table* t, long long n_bags, long long nnz) {
   L.n_regions = (unsigned)t->st.n_slots + 1;  // one per slot, then the absent region
   // every region adds at most one partial tile
   L.n_tiles_sort = (unsigned)((n + kSortTile - 1) / kSortTile) + L.n_regions;
-  L.n_chunks = (unsigned)((n + kChunk - 1) / kChunk);
+  // sub-chunk length: 256 positions, halved down to 32 while that leaves
+  // fewer than about 64 sub-chunks per SM (a small batch then still spreads
+  // over every SM instead of a few groups walking long sub-chunks in turn)
+  L.chunk = kChunk;
+  while (L.chunk > kMinChunk && n < (size_t)L.chunk * 64 * (size_t)sm_count()) L.chunk >>= 1;
+  L.n_chunks = (unsigned)((n + L.chunk - 1) / L.chunk);
   const size_t n_counts = (size_t)kDigits * L.n_tiles_sort;
   const size_t scan_n = std::max(std::max(n_counts, n), nb);
   L.n_scan_partials = (unsigned)((scan_n + kScanTile - 1) / kScanTile);
@@ -860,7 +867,7 @@ struct StageMeta {
   int flags;  // bit0: segment starts in this sub-chunk, bit1: ends in it
 };
 
-// One lane group of G lanes streams a sub-chunk of kChunk sorted positions;
+// One lane group of G lanes streams a sub-chunk of `chunk` sorted positions;
 // each lane owns VW-float column vectors (NCB of them) of the row.  Per
 // window of G positions the lanes first work in parallel, one position each:
 // row, bag, merged run of equal (row, bag) neighbours, its weight (1/L times
@@ -896,7 +903,8 @@ template <typename TW, int G, int VW, int NCB, int U, bool kAllCols, typename Op
 __global__ void __launch_bounds__(kRedWarps * 32, 8) segreduce_update_kernel(
     TableView t, const unsigned* __restrict__ K, const unsigned* __restrict__ V, const float* __restrict__ scale,
     int mean, const float* __restrict__ grad, const float* __restrict__ zrow, unsigned n, unsigned n_bags,
-    unsigned n_chunks, float* __restrict__ partA, float* __restrict__ partB, unsigned* __restrict__ arow, Opt opt,
+    unsigned n_chunks, unsigned chunk, float* __restrict__ partA, float* __restrict__ partB,
+    unsigned* __restrict__ arow, Opt opt,
     unsigned* __restrict__ work) {
   constexpr int P = 32 / G;
   constexpr int CW = G * VW * NCB;      // columns a group covers
@@ -926,8 +934,8 @@ __global__ void __launch_bounds__(kRedWarps * 32, 8) segreduce_update_kernel(
   };
   const unsigned c_first = work ? next_chunk(0) : ((blockIdx.x * blockDim.x + threadIdx.x) >> 5) * P + sub;
   for (unsigned c = c_first; c < n_chunks; c = next_chunk(c)) {
-    const unsigned cs = c * kChunk;
-    const unsigned ce = min(cs + kChunk, n);
+    const unsigned cs = c * chunk;
+    const unsigned ce = min(cs + chunk, n);
     const unsigned before = cs > 0 ? K[cs - 1] : kNoRow;
     const bool first_starts = K[cs] != before;
     const bool last_ends = ce >= n || K[ce] != K[ce - 1];
@@ -1095,7 +1103,8 @@ __global__ void __launch_bounds__(kRedWarps * 32, 8) segreduce_update_kernel(
 
 template <typename TW, int G, int NCB, typename Opt>
 __global__ void __launch_bounds__(256) fixup_kernel(TableView t, const unsigned* __restrict__ K, unsigned n,
-                                                    unsigned n_chunks, const float* __restrict__ partA,
+                                                    unsigned n_chunks, unsigned chunk,
+                                                    const float* __restrict__ partA,
                                                     const float* __restrict__ partB,
                                                     const unsigned* __restrict__ arow, Opt opt) {
   constexpr int P = 32 / G;
@@ -1110,15 +1119,15 @@ __global__ void __launch_bounds__(256) fixup_kernel(TableView t, const unsigned*
     // row continues into chunk c + 1 because chunk c left a head partial).
     // Exponential search from c + 1: most such rows end in the next chunk.
     unsigned lo = c + 1, step = 1, probe_c = c + 2;
-    while (probe_c < n_chunks && K[(size_t)probe_c * kChunk] == row) {
+    while (probe_c < n_chunks && K[(size_t)probe_c * chunk] == row) {
       lo = probe_c;
       step <<= 1;
       probe_c = lo + step;
     }
-    unsigned hi = min(probe_c, n_chunks) - 1;  // K[lo * kChunk] == row, answer in [lo, hi]
+    unsigned hi = min(probe_c, n_chunks) - 1;  // K[lo * chunk] == row, answer in [lo, hi]
     while (lo < hi) {
       const unsigned mid = lo + (hi - lo + 1) / 2;
-      if (K[(size_t)mid * kChunk] == row) lo = mid; else hi = mid - 1;
+      if (K[(size_t)mid * chunk] == row) lo = mid; else hi = mid - 1;
     }
     const unsigned c1 = lo;  // partials: A[c], B[c+1..c1]
     int D, col;
@@ -1269,14 +1278,14 @@ static cudaError_t launch_reduce(const emb_table* t, const unsigned* K, const un
   e = cudaMemsetAsync(work, 0, sizeof(unsigned), st);
   if (e != cudaSuccess) return e;
   kern<<<(int)std::max(1LL, blocks), threads, 0, st>>>(
-      v, K, V, scale, mean, grad, zrow, n, n_bags, L.n_chunks, pa, pb, ar, opt, work);
+      v, K, V, scale, mean, grad, zrow, n, n_bags, L.n_chunks, L.chunk, pa, pb, ar, opt, work);
   mark_phase(t, 2, st);
   // the fixup reads partial rows four columns per lane
   constexpr int G4 = G * VW / 4 > 32 ? 32 : G * VW / 4;
   constexpr int NCB4 = (G * VW * NCB) / (4 * G4);
   long long fblocks = std::min<long long>(((long long)L.n_chunks * 32 + 255) / 256, resident_blocks(256));
-  fixup_kernel<TW, G4, NCB4, Opt><<<(int)std::max(1LL, fblocks), 256, 0, st>>>(v, K, n, L.n_chunks, pa, pb, ar,
-                                                                                   opt);
+  fixup_kernel<TW, G4, NCB4, Opt><<<(int)std::max(1LL, fblocks), 256, 0, st>>>(v, K, n, L.n_chunks, L.chunk, pa,
+                                                                                   pb, ar, opt);
   mark_phase(t, 3, st);
   return cudaGetLastError();
 }

@@ -105,7 +105,10 @@ def test_failed_create_returns_oom_and_leaves_nothing_allocated():
     """Fault injection on the host: the table's first device allocation fails;
     create must return EMB_ERR_OOM (not abort) and hold no device memory.
     Nothing reaches CUDA, so this runs without a GPU."""
+    import gc
     keys = torch.tensor([(0 << 48) | 5, (1 << 48) | 7], dtype=torch.int64)
+    gc.collect()
+    gc.disable()
     live0 = E.emb_debug_live_device_allocs()
     E.emb_debug_fail_device_alloc(0)
     try:
@@ -113,5 +116,6 @@ def test_failed_create_returns_oom_and_leaves_nothing_allocated():
             E.emb_table_create([8, 8], "f32", keys, capacity=8, stream=0)   # no torch stream on a CPU machine
     finally:
         E.emb_debug_fail_device_alloc(-1)
+        gc.enable()
     assert ei.value.name == "EMB_ERR_OOM"
     assert E.emb_debug_live_device_allocs() == live0

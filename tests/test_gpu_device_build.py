@@ -5,6 +5,8 @@ the export and a forward), and the same errors.  Besides the five workloads'
 tables (scaled), tables built from keys chosen by their hash: many homes just
 before the end of the table (the layout wraps), runs longer than one warp
 replays, and a run longer than the device build takes."""
+import gc
+
 import numpy as np
 import pytest
 import torch
@@ -151,10 +153,17 @@ def test_device_build_errors_match_the_host(case):
         keys[4000] = -1
     with pytest.raises(E.EmbError) as eh:
         E.emb_table_plan([8], "f32", keys)
-    live0 = E.emb_debug_live_device_allocs()
-    with pytest.raises(E.EmbError) as ed:
-        E.emb_table_create_device([8], "f32", torch.from_numpy(keys).cuda())
+    keys_d = torch.from_numpy(keys).cuda()
+    gc.collect()                      # tables of earlier tests are freed now, not during the count
+    gc.disable()
+    try:
+        live0 = E.emb_debug_live_device_allocs()
+        with pytest.raises(E.EmbError) as ed:
+            E.emb_table_create_device([8], "f32", keys_d)
+        live1 = E.emb_debug_live_device_allocs()
+    finally:
+        gc.enable()
     assert ed.value.name == eh.value.name
     if case == "dup":
         assert ed.value.message == eh.value.message              # the same keys-array index
-    assert E.emb_debug_live_device_allocs() == live0            # nothing left allocated
+    assert live1 == live0                                       # nothing left allocated

@@ -8,6 +8,8 @@ is made to fault or hang):
   EMB_ERR_OOM and leave none of the library's device memory allocated, and the
   library must keep working afterwards.
 """
+import gc
+
 import numpy as np
 import pytest
 import torch
@@ -77,21 +79,27 @@ def test_allocation_failure_at_every_point_of_create(cfg, wdtype, host_values):
     vals = wl.values.float() if wd == "f16m" else wl.values
     vals = vals.cpu() if host_values else vals.cuda()
     torch.cuda.synchronize()
-    live0 = E.emb_debug_live_device_allocs()
-    created_after = None
-    for after in range(0, 32):
-        E.emb_debug_fail_device_alloc(after)
-        try:
-            tbl = E.emb_table_create(cfg.dims, wd, wl.keys.cpu(), values=vals, capacity=cfg.capacity,
-                                     acc_init=cfg.acc0)
-        except E.EmbError as e:
-            assert e.name == "EMB_ERR_OOM", e
-            assert E.emb_debug_live_device_allocs() == live0, f"leak after failing allocation {after}"
-            continue
-        finally:
-            E.emb_debug_fail_device_alloc(-1)
-        created_after = after
-        break
+    keys_h = wl.keys.cpu()
+    gc.collect()                      # tables of earlier tests are freed now, not during the counts
+    gc.disable()
+    try:
+        live0 = E.emb_debug_live_device_allocs()
+        created_after = None
+        for after in range(0, 32):
+            E.emb_debug_fail_device_alloc(after)
+            try:
+                tbl = E.emb_table_create(cfg.dims, wd, keys_h, values=vals, capacity=cfg.capacity,
+                                         acc_init=cfg.acc0)
+            except E.EmbError as e:
+                assert e.name == "EMB_ERR_OOM", e
+                assert E.emb_debug_live_device_allocs() == live0, f"leak after failing allocation {after}"
+                continue
+            finally:
+                E.emb_debug_fail_device_alloc(-1)
+            created_after = after
+            break
+    finally:
+        gc.enable()
     assert created_after is not None and created_after >= 8      # every allocation point was failed once
     # the library still works: the table that was created runs a step
     off, q, g = wl.offsets, wl.qkeys, wl.grad
@@ -99,5 +107,9 @@ def test_allocation_failure_at_every_point_of_create(cfg, wdtype, host_values):
     ws = torch.empty(E.emb_bwd_workspace_size(tbl, off.numel() - 1, q.numel()), dtype=torch.uint8, device="cuda")
     E.emb_bwd_adagrad(tbl, off, q, cfg.pool, g, cfg.lr, cfg.eps, ws)
     assert E.emb_check_device_flag(tbl) == 0 and torch.isfinite(out).all()
-    tbl.close()
-    assert E.emb_debug_live_device_allocs() == live0
+    gc.disable()
+    try:
+        tbl.close()
+        assert E.emb_debug_live_device_allocs() == live0
+    finally:
+        gc.enable()
