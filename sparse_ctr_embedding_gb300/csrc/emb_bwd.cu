@@ -49,7 +49,7 @@ emb_status check_batch(const emb_table* t, const int64_t* offsets_d, int64_t n_b
                        int64_t nnz, int pool);
 cudaError_t launch_forward(const emb_table* t, const long long* offsets, long long n_bags, const long long* keys,
                            long long nnz, int mean, float* out, unsigned* K, unsigned* V, float* scale,
-                           const unsigned* dest, unsigned long long* work, cudaStream_t st);
+                           const unsigned* dest, const unsigned* placed, unsigned long long* work, cudaStream_t st);
 
 constexpr int kChunk = 256;                      // sorted positions per reduce sub-chunk (large batches)
 constexpr int kMinChunk = 32;                    // the shortest sub-chunk (small batches)
@@ -74,6 +74,7 @@ struct WsHeader {
   unsigned miss_row;         // sentinel row of a miss (= n_rows)
   unsigned n_unique;         // filled by emb_bwd_unique_keys
   unsigned long long total;  // sum of the (clamped) bag lengths: nnz unless the offsets are malformed
+  unsigned placed;           // 1: the clamped bags tile [0, nnz), pairs may be recorded
 };
 
 // One region of the sort: the pairs of one feature slot, or (the last region)
@@ -192,24 +193,24 @@ __global__ void __launch_bounds__(256) expand_kernel(TableView t, const long lon
 
 // ------------------------------------------------------------------ 2. radix sort
 
+// Lanes of the warp whose digit equals this lane's (invalid lanes form their
+// own group), with one match instruction: measured 5.74 ms for the sort at
+// 100M keys against 5.90 with one ballot per digit bit, 0.79 against 0.84
+// at 100 slots x dim 32.
+__device__ __forceinline__ unsigned warp_peers(unsigned d, bool valid) {
+  return __match_any_sync(0xffffffffu, valid ? d : 0xFFFFFFFFu);
+}
+
 // Stable per-warp ranking over one tile: each warp walks its 32*kSortItems
-// consecutive keys in order, 32 at a time; lanes holding the same digit are
-// found with one ballot per digit bit, and the group leader bumps the warp's
-// counter.  Returns, per item, its rank among equal digits of this warp.
+// consecutive keys in order, 32 at a time; the lowest lane of each group of
+// equal digits bumps the warp's counter for that digit.  Returns, per item,
+// its rank among equal digits of this warp.
 __device__ __forceinline__ void warp_rank(unsigned (&d)[kSortItems], unsigned (&rank)[kSortItems], bool (&valid)[kSortItems],
                                           unsigned* cnt /* this warp's kDigits counters */) {
   const int lane = threadIdx.x & 31;
 #pragma unroll
   for (int r = 0; r < kSortItems; ++r) {
-    // lanes holding the same digit: one ballot per digit bit, plus validity
-    const unsigned vb = __ballot_sync(0xffffffffu, valid[r]);
-    unsigned peers = valid[r] ? vb : ~vb;
-#pragma unroll
-    for (int b = 0; b < kRadixBits; ++b) {
-      const unsigned bit = (d[r] >> b) & 1u;
-      const unsigned bb = __ballot_sync(0xffffffffu, bit);
-      peers &= bit ? bb : ~bb;
-    }
+    const unsigned peers = warp_peers(d[r], valid[r]);
     const int leader = __ffs(peers) - 1;
     unsigned base = 0;
     if (valid[r] && lane == leader) {
@@ -595,6 +596,7 @@ __global__ void __launch_bounds__(1024) seg_setup_kernel(TableView t, WsHeader* 
     hdr->sorted_in_b = sorted_in_b;
     hdr->miss_row = t.n_rows;
     hdr->n_unique = 0;
+    hdr->placed = placed ? 1u : 0u;
     carry = 0;
     if (!placed && nnz > 0) atomicOr(t.flags, EMB_FLAG_BAD_OFFSETS);
   }
@@ -1683,7 +1685,8 @@ emb_status emb_lookup_fwd_record(emb_table* table, const int64_t* offsets_d, int
     EMB_CUDA(cudaMemsetAsync(fwork, 0, sizeof(unsigned long long), st));
     cudaError_t e = launch_forward(table, (const long long*)offsets_d, n_bags, (const long long*)keys_d, nnz,
                                    pool == EMB_POOL_MEAN, out_d, (unsigned*)(ws + L.kA), (unsigned*)(ws + L.vA),
-                                   (float*)(ws + L.scale), (const unsigned*)(ws + L.dest), fwork, st);
+                                   (float*)(ws + L.scale), (const unsigned*)(ws + L.dest),
+                                   &((const WsHeader*)(ws + L.hdr))->placed, fwork, st);
     if (e != cudaSuccess) return cuda_fail(e, "fwd_pool_kernel launch");
   }
   EMB_CUDA(cudaGetLastError());

@@ -6,13 +6,16 @@
 // per-sample bags pooled by sum or mean.
 //
 // Mapping (one launch for every slot and dim): one team of TEAM lanes (8, 16
-// or 32: a warp holds 32/TEAM teams) per bag, grid-stride over bags in CSR
-// order.  The team resolves up to TEAM keys of the bag at once (one key per
-// lane: their probes are in flight together), then its lanes split into
-// P = TEAM/G groups of G lanes; group p pools keys p, p+P, ...
-// of the chunk, each lane owning 16-byte column vectors of the row.  U keys
-// per group are gathered before any is added, so every lane keeps U x NCB
-// 16-byte loads in flight.  The P partial sums are combined with xor
+// or 32: a warp holds 32/TEAM teams) per bag.  The plain forward walks the
+// bags grid-stride in CSR order; the recording forward takes them 32 at a
+// time from a device counter in slot-major order (every sample of slot 0,
+// then slot 1, ...), staging the batch's checked CSR bounds and pair
+// positions in shared memory.  The team resolves up to TEAM keys of the bag
+// at once (one key per lane: their probes are in flight together), then its
+// lanes split into P = TEAM/G groups of G lanes; group p pools keys p, p+P,
+// ... of the chunk, each lane owning 16-byte column vectors of the row.  U
+// keys per group are gathered before any is added, so every lane keeps
+// U x NCB 16-byte loads in flight.  The P partial sums are combined with xor
 // shuffles and group 0 writes the pooled row with 16-byte stores.
 // Accumulation is float32 in a fixed order, so results are deterministic.
 #include <algorithm>
@@ -81,52 +84,87 @@ struct Record {
   unsigned* V;
   float* scale;
   const unsigned* dest;      // first position of each bag's pairs, slot-major: dest[s * B + b]
+  const unsigned* placed;    // nonzero when the bags tile [0, nnz) (else nothing is recorded)
   unsigned long long B;      // samples in the batch
   unsigned long long* work;  // optional bag counter: bags taken in batches, in order
+  int slot_major;            // with work: the counter runs over t = s * B + b instead of bag = b * S + s
 };
 
 constexpr int kBagBatch = 32;  // bags per counter increment
 
-// Bounded to 8 resident blocks (full occupancy): the gathers are latency
-// bound, and resident warps beat registers (measured at 100M keys x dim 128).
+// Resident 256-thread blocks per SM the register budget is sized for, by team
+// width.  The gathers are latency bound, so occupancy and spill-free registers
+// trade against each other; measured per team width on the five benchmark
+// workloads: 8-lane teams (100 slots x dim 32 f16) run best at 4 blocks of
+// 64 registers (1.74 ms against 2.01 at 8 blocks of 32), 16-lane teams
+// (26 slots x dim 64 f32) at 6 (0.320 ms against 0.376), 32-lane teams
+// (100M keys x dim 128 f16; the ragged one) at 8 (12.08 ms against 12.17 at
+// 6 and 13.95 at 4).
+constexpr int fwd_min_blocks(int team) { return team == 8 ? 4 : team == 16 ? 6 : 8; }
+constexpr unsigned kMissRow = 0xFFFFFFFFu;
+
+// Indices are 32-bit: n_bags and nnz are below 2^31 (the boundary checks it),
+// so bag numbers, CSR positions and pair positions all fit.
 template <typename TW, int TEAM, int NCB, int U, bool kRecord>
-__global__ void __launch_bounds__(256, 8) fwd_pool_kernel(TableView t, const long long* __restrict__ offsets,
-                                                       long long n_bags, const long long* __restrict__ keys,
-                                                       long long nnz, int mean, float* __restrict__ out, Record rec) {
+__global__ void __launch_bounds__(256, fwd_min_blocks(TEAM)) fwd_pool_kernel(TableView t, const long long* __restrict__ offsets,
+                                                                      long long n_bags_l,
+                                                                      const long long* __restrict__ keys,
+                                                                      long long nnz_l, int mean, float* __restrict__ out,
+                                                                      Record rec) {
   constexpr int VEC = VecOf<TW>::kElems;
   constexpr int BPW = 32 / TEAM;  // bags a warp works on side by side
+  const unsigned n_bags = (unsigned)n_bags_l, nnz = (unsigned)nnz_l;
   const int lane = threadIdx.x & 31;
   const int team = lane / TEAM, tl = lane % TEAM;
   const unsigned tmask = TEAM == 32 ? 0xffffffffu : (((1u << TEAM) - 1u) << (team * TEAM));
-  const long long nteams = (((long long)gridDim.x * blockDim.x) >> 5) * BPW;
+  const unsigned S = (unsigned)t.n_slots;
+  const unsigned B = (unsigned)rec.B;
+  const bool by_slot = rec.work != nullptr && rec.slot_major != 0;
+  const unsigned nteams = ((gridDim.x * blockDim.x) >> 5) * BPW;
   const TW* W = static_cast<const TW*>(t.W);
   const int G0 = t.uniform_dim ? min(TEAM, pow2_at_least(t.uniform_dim / VEC)) : 0;  // lanes per key, one dim
-  // bags: a static grid-stride order, or batches of kBagBatch consecutive bags
-  // taken in order from a counter (balances warps over bags of very
-  // different lengths)
-  long long stat = ((blockIdx.x * (long long)blockDim.x + threadIdx.x) >> 5) * BPW + team;
-  // CSR offsets (and, recording, the pairs' slot-major positions) of a team's
-  // batch of bags, staged in shared memory with one load per lane: each bag
-  // then starts its key -> slot -> row chain without two dependent global reads
-  __shared__ long long s_off[8][BPW][kBagBatch + 1];
+  // bags: a static grid-stride order, or batches of kBagBatch consecutive
+  // counter values taken in order (balances warps over bags of very
+  // different lengths); a counter value is a bag number, or with by_slot the
+  // slot-major number s * B + b of bag b * S + s
+  unsigned stat = ((blockIdx.x * blockDim.x + threadIdx.x) >> 5) * BPW + team;
+  // Checked and clamped CSR bounds (start << 32 | end) and, when recording,
+  // the pairs' slot-major positions of a team's batch of bags, staged in
+  // shared memory by the lanes in parallel: each bag then starts its
+  // key -> slot -> row chain without two dependent global reads
+  __shared__ unsigned long long s_se[8][BPW][kBagBatch];
   __shared__ unsigned s_dst[8][BPW][kBagBatch];
   const int wib = threadIdx.x >> 5;
+  // malformed offsets whose clamped bags do not tile [0, nnz) record nothing
+  // (the backward then updates nothing); otherwise every position is in range
+  const bool recording = kRecord && *rec.placed != 0;
   for (;;) {
-    long long b_lo, b_hi;
+    unsigned b_lo, b_hi;
     if (rec.work) {
       unsigned long long v = 0;
       if (tl == 0) v = atomicAdd(rec.work, (unsigned long long)kBagBatch);
-      b_lo = (long long)__shfl_sync(tmask, v, 0, TEAM);  // also: the team is done with the last batch
-      b_hi = min(b_lo + kBagBatch, n_bags);
+      // below n_bags + 32 x teams < 2^32; also: the team is done with the last batch
+      b_lo = (unsigned)__shfl_sync(tmask, v, 0, TEAM);
+      b_hi = min(b_lo + (unsigned)kBagBatch, n_bags);
       if (b_lo < n_bags) {
         const int nb = (int)(b_hi - b_lo);
-        for (int j = tl; j <= nb; j += TEAM) s_off[wib][team][j] = offsets[b_lo + j];
-        if (kRecord)
-          for (int j = tl; j < nb; j += TEAM) {
-            const unsigned bj = (unsigned)(b_lo + j);
-            s_dst[wib][team][j] = rec.dest[(unsigned long long)(bj % (unsigned)t.n_slots) * rec.B +
-                                           bj / (unsigned)t.n_slots];
+        for (int j = tl; j < nb; j += TEAM) {
+          const unsigned tj = b_lo + j;
+          unsigned bag = tj;
+          if (by_slot) {
+            const unsigned ss = tj / B;
+            bag = (tj - ss * B) * S + ss;
           }
+          long long start = offsets[bag], end = offsets[bag + 1];
+          if (start < 0 || end > (long long)nnz || end < start || (bag == 0 && start != 0) ||
+              (bag == n_bags - 1 && end != (long long)nnz)) {
+            atomicOr(t.flags, EMB_FLAG_BAD_OFFSETS);
+            start = min(max(start, 0LL), (long long)nnz);
+            end = min(max(end, start), (long long)nnz);
+          }
+          s_se[wib][team][j] = ((unsigned long long)start << 32) | (unsigned long long)end;
+          if (kRecord) s_dst[wib][team][j] = rec.dest[by_slot ? tj : (bag % S) * B + bag / S];
+        }
       }
       __syncwarp(tmask);
     } else {
@@ -135,72 +173,77 @@ __global__ void __launch_bounds__(256, 8) fwd_pool_kernel(TableView t, const lon
       stat += nteams;
     }
     if (b_lo >= n_bags) break;
-  for (long long bag = b_lo; bag < b_hi; ++bag) {
-    const int s = (int)((unsigned)bag % (unsigned)t.n_slots);
-    const long long b = (unsigned)bag / (unsigned)t.n_slots;
+  for (unsigned tt = b_lo; tt < b_hi; ++tt) {
+    unsigned s, b;
+    if (by_slot) {
+      s = tt / B;
+      b = tt - s * B;
+    } else {
+      b = tt / S;
+      s = tt - b * S;
+    }
+    const unsigned bag = b * S + s;
     int D, col;
-    long long ebase = 0;
-    unsigned rbase = 0;
+    const TW* Wb = W;    // the slot's first row
+    unsigned rbase = 0;  // and its internal row number
     if (t.uniform_dim) {
       D = t.uniform_dim;
-      col = s * D;
+      col = (int)s * D;
     } else {
       const SlotInfo si = t.sinfo[s];
       D = si.dim;
       col = si.col;
-      ebase = si.elem_base;
+      Wb = W + si.elem_base;
       rbase = si.row_base;
     }
     const int G = t.uniform_dim ? G0 : min(TEAM, pow2_at_least(D / VEC));  // lanes per key
     const int P = TEAM / G;                           // keys pooled side by side
     const int sub = tl / G, li = tl % G;
 
-    long long start, end;
-    if (rec.work) {
-      start = s_off[wib][team][bag - b_lo];
-      end = s_off[wib][team][bag - b_lo + 1];
+    unsigned start, end;
+    if (rec.work) {  // checked when staged
+      const unsigned long long se = s_se[wib][team][tt - b_lo];
+      start = (unsigned)(se >> 32);
+      end = (unsigned)se;
     } else {
-      start = offsets[bag];
-      end = offsets[bag + 1];
+      long long st = offsets[bag], en = offsets[bag + 1];
+      if (st < 0 || en > (long long)nnz || en < st || (bag == 0 && st != 0) ||
+          (bag == n_bags - 1 && en != (long long)nnz)) {
+        if (tl == 0) atomicOr(t.flags, EMB_FLAG_BAD_OFFSETS);
+        st = min(max(st, 0LL), (long long)nnz);
+        en = min(max(en, st), (long long)nnz);
+      }
+      start = (unsigned)st;
+      end = (unsigned)en;
     }
-    if (start < 0 || end > nnz || end < start || (bag == 0 && start != 0) || (bag == n_bags - 1 && end != nnz)) {
-      if (tl == 0) atomicOr(t.flags, EMB_FLAG_BAD_OFFSETS);
-      start = min(max(start, 0LL), nnz);
-      end = min(max(end, start), nnz);
-    }
-    // where this bag's pairs go (inside [0, nnz) unless the offsets are malformed)
-    const long long d0 =
-        kRecord ? (long long)(rec.work ? s_dst[wib][team][bag - b_lo]
-                                       : rec.dest[(unsigned long long)s * rec.B + (unsigned long long)b]) - start
-                : 0;
+    // where this bag's pairs go (inside [0, nnz) when recording)
+    const unsigned dst = kRecord ? (rec.work ? s_dst[wib][team][tt - b_lo] : rec.dest[s * B + b]) : 0u;
     float acc[NCB][VEC];
 #pragma unroll
     for (int c = 0; c < NCB; ++c)
 #pragma unroll
       for (int j = 0; j < VEC; ++j) acc[c][j] = 0.f;
 
-    for (long long c0 = start; c0 < end; c0 += TEAM) {
-      const int n = (int)min((long long)TEAM, end - c0);
-      long long elem = -1;  // first weight element of this lane's key, -1 = miss
+    for (unsigned c0 = start; c0 < end; c0 += TEAM) {
+      const int n = (int)min((unsigned)TEAM, end - c0);
+      unsigned rr = kMissRow;  // row of this lane's key within its slot's rows
       if (tl < n) {
         const long long k = keys[c0 + tl];
         unsigned row = t.n_rows;
-        if (key_slot(k) != s) {
+        if (key_slot(k) != (int)s) {
           atomicOr(t.flags, EMB_FLAG_SLOT_MISMATCH);
         } else {
           unsigned r, ext;
           unsigned long long h;
           if (probe(t, k, &r, &ext, &h)) {
             row = r;
-            elem = t.uniform_dim ? (long long)r * D : ebase + (long long)(r - rbase) * D;
+            rr = r - rbase;
           }
         }
-        if (kRecord) {
-          const long long p = d0 + c0 + tl;
-          if (p < nnz) {
-            rec.K[p] = row;
-            rec.V[p] = (unsigned)bag;
-          }
+        if (recording) {  // the bags tile [0, nnz): the position is inside it
+          const unsigned p = dst + (c0 - start) + tl;
+          rec.K[p] = row;
+          rec.V[p] = bag;
         }
       }
       for (int base = 0; base < n; base += P * U) {
@@ -208,12 +251,13 @@ __global__ void __launch_bounds__(256, 8) fwd_pool_kernel(TableView t, const lon
 #pragma unroll
         for (int u = 0; u < U; ++u) {
           const int i = base + u * P + sub;
-          const long long e = __shfl_sync(tmask, elem, i & (TEAM - 1), TEAM);
-          const bool ok = (i < n) && (e >= 0);
+          const unsigned ri = __shfl_sync(tmask, rr, i & (TEAM - 1), TEAM);
+          const bool ok = (i < n) && (ri != kMissRow);
+          const TW* rp = Wb + (size_t)ri * (unsigned)D;
 #pragma unroll
           for (int c = 0; c < NCB; ++c) {
             const int ce = (c * G + li) * VEC;
-            v[u][c] = (ok && ce < D) ? ldg16(W + e + ce) : make_uint4(0u, 0u, 0u, 0u);
+            v[u][c] = (ok && ce < D) ? ldg16(rp + ce) : make_uint4(0u, 0u, 0u, 0u);
           }
         }
 #pragma unroll
@@ -231,11 +275,11 @@ __global__ void __launch_bounds__(256, 8) fwd_pool_kernel(TableView t, const lon
 
     if (kRecord && mean && tl == 0) rec.scale[bag] = end > start ? 1.0f / (float)(end - start) : 0.f;
     if (sub == 0) {
-      const long long L = end - start;
+      const unsigned L = end - start;
       // mean over L counting misses, as one reciprocal times each sum (within
       // one rounding of the quotient); L = 0 gives 0
       const float inv = (mean && L > 0) ? 1.f / (float)L : 1.f;
-      float* o = out + b * t.sum_dims + col;
+      float* o = out + (size_t)b * (unsigned)t.sum_dims + col;
 #pragma unroll
       for (int c = 0; c < NCB; ++c) {
         const int ce = (c * G + li) * VEC;
@@ -305,8 +349,16 @@ static cudaError_t launch_fwd(const emb_table* t, const long long* offsets, long
 // Forward launch, optionally recording (row, bag) pairs for the backward.
 cudaError_t launch_forward(const emb_table* t, const long long* offsets, long long n_bags, const long long* keys,
                            long long nnz, int mean, float* out, unsigned* K, unsigned* V, float* scale,
-                           const unsigned* dest, unsigned long long* work, cudaStream_t st) {
-  const Record rec{K, V, scale, dest, (unsigned long long)n_bags / (unsigned long long)t->st.n_slots, work};
+                           const unsigned* dest, const unsigned* placed, unsigned long long* work, cudaStream_t st) {
+  // The recording forward takes bags in slot-major order (all samples of
+  // slot 0, then slot 1, ...): the gathers then stay inside one slot's block
+  // of rows at a time and the recorded pairs are written in place order.
+  // Measured: 12.08 ms against 14.15 in sample-major order at 100M keys x
+  // dim 128 f16, 2.01 against 2.21 at 100 slots x dim 32 f16, within 0.01 ms
+  // on the smaller workloads.
+  const int slot_major = work != nullptr ? 1 : 0;
+  const Record rec{K,    V, scale, dest, placed, (unsigned long long)n_bags / (unsigned long long)t->st.n_slots,
+                   work, slot_major};
   const bool record = K != nullptr;
   if (t->fwd_half())
     return record ? launch_fwd<__half, true>(t, offsets, n_bags, keys, nnz, mean, out, rec, st)
@@ -340,7 +392,8 @@ extern "C" emb_status emb_lookup_fwd(emb_table* table, const int64_t* offsets_d,
   if (((uintptr_t)out_d & 15) != 0) return fail(EMB_ERR_INVALID_ARG, "out must be 16-byte aligned");
   cudaStream_t st = (cudaStream_t)stream;
   cudaError_t e = launch_forward(table, (const long long*)offsets_d, n_bags, (const long long*)keys_d, nnz,
-                                 pool == EMB_POOL_MEAN, out_d, nullptr, nullptr, nullptr, nullptr, nullptr, st);
+                                 pool == EMB_POOL_MEAN, out_d, nullptr, nullptr, nullptr, nullptr, nullptr, nullptr,
+                                 st);
   if (e != cudaSuccess) return cuda_fail(e, "fwd_pool_kernel launch");
   return EMB_OK;
 }
