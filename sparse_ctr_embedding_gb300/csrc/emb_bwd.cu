@@ -51,8 +51,9 @@ cudaError_t launch_forward(const emb_table* t, const long long* offsets, long lo
                            long long nnz, int mean, float* out, unsigned* K, unsigned* V, float* scale,
                            const unsigned* dest, const unsigned* placed, unsigned long long* work, cudaStream_t st);
 
-constexpr int kChunk = 256;                      // sorted positions per reduce sub-chunk (large batches)
+constexpr int kChunk = 256;                      // sorted positions per reduce sub-chunk (the largest batches)
 constexpr int kMinChunk = 32;                    // the shortest sub-chunk (small batches)
+constexpr size_t kLongChunkFrom = size_t(1) << 27;  // positions from which sub-chunks are kChunk long
 constexpr int kSortWarps = 8;
 constexpr int kSortThreads = kSortWarps * 32;
 constexpr int kSortItems = 16;                   // keys per lane per tile
@@ -104,10 +105,13 @@ static WsLayout ws_layout(const emb_table* t, long long n_bags, long long nnz) {
   L.n_regions = (unsigned)t->st.n_slots + 1;  // one per slot, then the absent region
   // every region adds at most one partial tile
   L.n_tiles_sort = (unsigned)((n + kSortTile - 1) / kSortTile) + L.n_regions;
-  // sub-chunk length: 256 positions, halved down to 32 while that leaves
-  // fewer than about 64 sub-chunks per SM (a small batch then still spreads
-  // over every SM instead of a few groups walking long sub-chunks in turn)
-  L.chunk = kChunk;
+  // sub-chunk length: 256 positions from 2^27 positions up, else 128 (measured
+  // per workload: at 282M positions 128 doubles the fixup, +0.6 ms; at 36M,
+  // 6.5M and 4.5M positions it saves 0.07, 0.03 and 0.06 ms of reduce plus
+  // fixup), halved down to 32 while that leaves fewer than about 64
+  // sub-chunks per SM (a small batch then still spreads over every SM
+  // instead of a few groups walking long sub-chunks in turn)
+  L.chunk = n >= kLongChunkFrom ? kChunk : kChunk / 2;
   while (L.chunk > kMinChunk && n < (size_t)L.chunk * 64 * (size_t)sm_count()) L.chunk >>= 1;
   L.n_chunks = (unsigned)((n + L.chunk - 1) / L.chunk);
   const size_t n_counts = (size_t)kDigits * L.n_tiles_sort;
@@ -213,10 +217,9 @@ __device__ __forceinline__ void warp_rank(unsigned (&d)[kSortItems], unsigned (&
     const unsigned peers = warp_peers(d[r], valid[r]);
     const int leader = __ffs(peers) - 1;
     unsigned base = 0;
-    if (valid[r] && lane == leader) {
-      base = cnt[d[r]];
-      cnt[d[r]] = base + __popc(peers);
-    }
+    // one shared atomic per group (the counter's old value): successive
+    // items' updates pipeline instead of chaining a load and a store
+    if (valid[r] && lane == leader) base = atomicAdd(&cnt[d[r]], (unsigned)__popc(peers));
     base = __shfl_sync(0xffffffffu, base, leader);
     rank[r] = base + __popc(peers & lanemask_lt());
     __syncwarp();
@@ -350,8 +353,7 @@ __global__ void __launch_bounds__(kSortThreads, 3) radix_scatter_kernel(
   extern __shared__ unsigned smem[];
   unsigned(*cnt)[kDigits] = reinterpret_cast<unsigned(*)[kDigits]>(smem);  // [kSortWarps][kDigits]
   unsigned* gbase = smem + kSortWarps * kDigits;                             // [kDigits]
-  unsigned* bstart = gbase + kDigits;                                         // [kDigits]
-  unsigned* wtot = bstart + kDigits;                                          // [33]
+  unsigned* wtot = gbase + kDigits;                                           // [33]
   unsigned* tk = wtot + 33;                                                   // [kSortTile]
   unsigned* tv = tk + kSortTile;                                              // [kSortTile]
   __shared__ unsigned reg;
@@ -407,7 +409,7 @@ __global__ void __launch_bounds__(kSortThreads, 3) radix_scatter_kernel(
   for (int j = 0; j < kPer; ++j) {
     const int dg = threadIdx.x * kPer + j;
     if (dg < kDigits) {
-      bstart[dg] = excl;
+      gbase[dg] -= excl;  // now output position minus tile position for the digit
 #pragma unroll
       for (int ww = 0; ww < kSortWarps; ++ww) cnt[ww][dg] += excl;
       excl += run[j];
@@ -427,7 +429,7 @@ __global__ void __launch_bounds__(kSortThreads, 3) radix_scatter_kernel(
   for (unsigned j = threadIdx.x; j < tile_n; j += kSortThreads) {
     const unsigned kk = tk[j];
     const unsigned dg = region_digit(g, kk, shift);
-    const unsigned gp = gbase[dg] + (j - bstart[dg]);
+    const unsigned gp = gbase[dg] + j;
     kout[gp] = kk;
     vout[gp] = tv[j];
   }
@@ -1242,7 +1244,7 @@ cudaError_t launch_scan_u32(const unsigned* in, unsigned* out, size_t n, unsigne
 }
 
 static size_t scatter_smem() {
-  return sizeof(unsigned) * ((size_t)kSortWarps * kDigits + 2 * kDigits + 33 + 2 * (size_t)kSortTile);
+  return sizeof(unsigned) * ((size_t)kSortWarps * kDigits + kDigits + 33 + 2 * (size_t)kSortTile);
 }
 
 // Record the caller's timing event for a finished backward phase, if any.
