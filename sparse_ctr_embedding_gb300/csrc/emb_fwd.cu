@@ -336,9 +336,11 @@ static cudaError_t launch_fwd(const emb_table* t, const long long* offsets, long
   } else if (team == 16) {
     if (ncb <= 1) EMB_FWD(16, 1, 4); else EMB_FWD(16, 2, 2);
   } else {
-    // 3 rows in flight per lane: 14.0 ms against 14.9 (4) and 14.5 (2) at
-    // 100M keys x dim 128 f16; 0.385 ms against 0.407 (4) at 10M x dim 64 f32
-    if (ncb <= 1) EMB_FWD(32, 1, 3);
+    // 1 row in flight per lane (2 per team): 11.17 ms against 11.22 (2),
+    // 12.05 (3) and 13.26 (4) at 100M keys x dim 128 f16; 0.651 ms against
+    // 0.671 (2) and 0.699 (3) on the ragged workload (fewer registers live
+    // at the 32-register budget: fewer spills)
+    if (ncb <= 1) EMB_FWD(32, 1, 1);
     else if (ncb <= 2) EMB_FWD(32, 2, 2);
     else EMB_FWD(32, 4, 1);
   }
