@@ -49,6 +49,8 @@ def parse():
     ap.add_argument("--ref-samples", type=int, default=128, help="samples per reference-arm step")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--pipeline-depth", type=int, default=2,
+                    help="buffer sets of the e2e leg's batch pipeline (uploads run up to depth - 1 batches ahead)")
     return ap.parse_args()
 
 
@@ -430,7 +432,7 @@ def run_ours(args):
         d2h = out_h.numel() * 4
         # the library's batch pipeline: uploads of the next batch (copy stream) and
         # the pooled output's download (second copy stream) overlap the step
-        pipe = E.Pipeline(tbl, n_bags, nnz, depth=2, upload_grad=True, stream=stream)
+        pipe = E.Pipeline(tbl, n_bags, nnz, depth=args.pipeline_depth, upload_grad=True, stream=stream)
 
         def run_e2e(n_steps):
             torch.cuda.synchronize()
@@ -451,7 +453,7 @@ def run_ours(args):
         e2e_ms = max_over_ranks(ws, run_e2e(Ke)) / Ke
         pipe.close()
         e2e = {"value": ws * nnz / (e2e_ms * 1e-3), "unit": "lookups/s", "ms_per_step": e2e_ms,
-               "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+               "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "pipeline_depth": args.pipeline_depth,
                "path": "emb_pipeline (C ABI): pinned host CSR batch + grad_out uploaded on the pipeline's copy "
                        "stream, recording forward + recorded backward on the compute stream, pooled output "
                        "downloaded on its second copy stream; host wall clock from the first upload to the "

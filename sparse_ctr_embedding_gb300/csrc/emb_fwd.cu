@@ -95,12 +95,12 @@ constexpr int kBagBatch = 32;  // bags per counter increment
 // Resident 256-thread blocks per SM the register budget is sized for, by team
 // width.  The gathers are latency bound, so occupancy and spill-free registers
 // trade against each other; measured per team width on the five benchmark
-// workloads: 8-lane teams (100 slots x dim 32 f16) run best at 4 blocks of
+// workloads: 4- and 8-lane teams (100 slots x dim 32 f16) run best at 4 blocks of
 // 64 registers (1.74 ms against 2.01 at 8 blocks of 32), 16-lane teams
 // (26 slots x dim 64 f32) at 6 (0.320 ms against 0.376), 32-lane teams
 // (100M keys x dim 128 f16; the ragged one) at 8 (12.08 ms against 12.17 at
 // 6 and 13.95 at 4).
-constexpr int fwd_min_blocks(int team) { return team == 8 ? 4 : team == 16 ? 6 : 8; }
+constexpr int fwd_min_blocks(int team) { return team <= 8 ? 4 : team == 16 ? 6 : 8; }
 constexpr unsigned kMissRow = 0xFFFFFFFFu;
 
 // Indices are 32-bit: n_bags and nnz are below 2^31 (the boundary checks it),
@@ -302,12 +302,17 @@ __global__ void __launch_bounds__(256, fwd_min_blocks(TEAM)) fwd_pool_kernel(Tab
 }
 
 // Lanes per bag: enough for the widest row's 16-byte vectors and for the
-// mean bag's keys to be probed at once, at least 8 and at most a warp.
-// Measured: 100 slots x dim 32 f16 with 5.5-key bags, 8 lanes 2.32 ms against
-// 4.40 ms for a warp per bag; 26 slots x dim 64 f32 with 10.5-key bags, 16
-// lanes 0.388 ms against 0.419; the 100M-key workload (33.7-key bags) and
-// the ragged one (rows up to 32 vectors) keep a whole warp.
-static int fwd_team(int max_vecs, double mean_len) {
+// mean bag's keys to be probed at once, at least 8 and at most a warp; rows
+// of at most 4 vectors on batches of at least 2^20 bags take 4 lanes (a key's
+// row is one 4-lane load; enough bags are in flight to hide the probes).
+// Measured: 100 slots x dim 32 f16 with 5.5-key bags, 4 lanes 1.53 ms against
+// 1.74 with 8 lanes and 4.40 with a warp per bag; 26 slots x dim 64 f32 with
+// 10.5-key bags, 16 lanes 0.388 ms against 0.419; the 100M-key workload
+// (33.7-key bags) and the ragged one (rows up to 32 vectors) keep a whole
+// warp; the 1024-bag workload (rows of 4 vectors) takes 0.127 ms with 8
+// lanes against 0.184 with 4.
+static int fwd_team(int max_vecs, double mean_len, long long n_bags) {
+  if (max_vecs <= 4 && n_bags >= (1LL << 20)) return 4;
   const int want = std::max(max_vecs, (int)std::ceil(mean_len));
   return want <= 8 ? 8 : want <= 16 ? 16 : 32;
 }
@@ -317,7 +322,7 @@ static cudaError_t launch_fwd(const emb_table* t, const long long* offsets, long
                               long long nnz, int mean, float* out, Record rec, cudaStream_t st) {
   constexpr int VEC = VecOf<TW>::kElems;
   const int max_vecs = t->st.max_dim / VEC;  // 16-byte vectors in the widest row
-  const int team = fwd_team(max_vecs, n_bags > 0 ? (double)nnz / (double)n_bags : 0.0);
+  const int team = fwd_team(max_vecs, n_bags > 0 ? (double)nnz / (double)n_bags : 0.0, n_bags);
   const int ncb = (max_vecs + team - 1) / team;  // column blocks per lane
   const int threads = 256;
   const long long want = std::max(1LL, (n_bags * team + threads - 1) / threads);
@@ -331,7 +336,9 @@ static cudaError_t launch_fwd(const emb_table* t, const long long* offsets, long
     fwd_pool_kernel<TW, TM, NC, UU, kRecord><<<(int)blocks, threads, 0, st>>>(v, offsets, n_bags, keys, nnz, mean, \
                                                                                out, rec);                   \
   } while (0)
-  if (team == 8) {
+  if (team == 4) {
+    EMB_FWD(4, 1, 4);
+  } else if (team == 8) {
     if (ncb <= 1) EMB_FWD(8, 1, 4); else EMB_FWD(8, 2, 2);
   } else if (team == 16) {
     if (ncb <= 1) EMB_FWD(16, 1, 4); else EMB_FWD(16, 2, 2);

@@ -1,7 +1,8 @@
 """GPU parity at the five workloads' full sizes, in the benchmark's launch
 configuration (the recording forward emb_lookup_fwd_record + the recorded
 backward emb_bwd_adagrad_recorded, as the benchmark times them; the
-unrecorded pair emb_lookup_fwd + emb_bwd_adagrad on the 26-slot workload),
+unrecorded pair emb_lookup_fwd + emb_bwd_adagrad on the 26-slot workload and
+on the 100-slot one, whose batch takes the 4-lane forward teams),
 on outputs the oracle computes one by one:
 
 * slot resolution and hit/miss: bit-exact on a random sample of occurrences;
@@ -93,7 +94,7 @@ class FullRun:
         self.tbl.close()
 
 
-@pytest.fixture(scope="module", params=[(1, True), (2, True), (2, False), (3, True), (4, True), (5, True)],
+@pytest.fixture(scope="module", params=[(1, True), (2, True), (2, False), (3, True), (3, False), (4, True), (5, True)],
                 ids=lambda p: f"config{p[0]}-{'recorded' if p[1] else 'unrecorded'}")
 def run(request):
     r = FullRun(*request.param)
