@@ -170,16 +170,18 @@ def max_over_ranks(ws, x: float) -> float:
     return float(t.item())
 
 
-def launches_per_step(max_slot_keys: int, digit_bits: int, dedup: bool = False) -> int:
+def launches_per_step(max_slot_keys: int, digit_bits: int, dedup: bool = False, nnz: int = 0) -> int:
     """Kernels this library launches for one forward (recording, or with dedupe) + one recorded bwd call.
-    The backward sorts rows within a slot, so the pass count follows the largest slot."""
+    The backward sorts rows within a slot, so the pass count follows the largest slot; the fold kernel
+    runs from 2^24 lookups."""
     bits = max(1, int(max_slot_keys).bit_length())
     passes = max(1, math.ceil(bits / digit_bits))
+    fold = 1 if nnz >= (1 << 24) else 0
     # placement (transpose + 3 scan kernels + region setup + tile map); recording fwd, or expand + the
-    # sort + dedupe pooling; (count + 3 scan + scatter) per radix pass; reduce; fixup
+    # sort + dedupe pooling; (count + 3 scan + scatter) per radix pass; reduce; fold; fixup
     if dedup:
-        return 6 + 1 + passes * 5 + 1 + 2
-    return 6 + 1 + passes * 5 + 2
+        return 6 + 1 + passes * 5 + 1 + 2 + fold
+    return 6 + 1 + passes * 5 + 2 + fold
 
 
 # ------------------------------------------------------------------ oracle (CPU baseline / reference arm)
@@ -502,7 +504,7 @@ def run_ours(args):
         "fwd_roofline": {"achieved": fwd_gbs, "frac": fwd_gbs / peak, "algorithmic_bytes": fwd_bytes},
         "bwd_roofline": {"achieved": bwd_gbs, "frac": bwd_gbs / peak, "algorithmic_bytes": bwd_bytes},
         "cpu_baseline": cpu, "e2e": e2e,
-        "gpu_launches": K * launches_per_step(st["max_slot_keys"], E.EMB_SORT_DIGIT_BITS, args.fwd == "dedup"),
+        "gpu_launches": K * launches_per_step(st["max_slot_keys"], E.EMB_SORT_DIGIT_BITS, args.fwd == "dedup", nnz),
         "clocks": clk, "device_flags": flags,
         "setup_s": {"generate": t_gen, "table_create": t_create, "table_create_device": t_create_dev},
     }

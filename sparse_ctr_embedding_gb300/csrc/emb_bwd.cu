@@ -54,6 +54,8 @@ cudaError_t launch_forward(const emb_table* t, const long long* offsets, long lo
 constexpr int kChunk = 256;                      // sorted positions per reduce sub-chunk (the largest batches)
 constexpr int kMinChunk = 32;                    // the shortest sub-chunk (small batches)
 constexpr size_t kLongChunkFrom = size_t(1) << 27;  // positions from which sub-chunks are kChunk long
+constexpr unsigned kFoldChunks = 32;             // sub-chunks per fold block (fixup of long rows)
+constexpr size_t kFoldFrom = size_t(1) << 24;     // positions from which the fold kernel runs
 constexpr int kSortWarps = 8;
 constexpr int kSortThreads = kSortWarps * 32;
 constexpr int kSortItems = 16;                   // keys per lane per tile
@@ -92,8 +94,9 @@ struct SortSeg {
 static size_t align_up(size_t x) { return (x + 255) & ~(size_t)255; }
 
 struct WsLayout {
-  size_t hdr, kA, kB, vA, vB, scale, dest, sseg, treg, counts, partials, partA, partB, arow, zero, work, fwork, uniq, total;
-  unsigned n_tiles_sort, n_regions, n_chunks, chunk, n_scan_partials;
+  size_t hdr, kA, kB, vA, vB, scale, dest, sseg, treg, counts, partials, partA, partB, partC, folded, arow, zero, work,
+      fwork, uniq, total;
+  unsigned n_tiles_sort, n_regions, n_chunks, chunk, n_scan_partials, n_fold;
   int max_dim;
 };
 
@@ -136,6 +139,9 @@ static WsLayout ws_layout(const emb_table* t, long long n_bags, long long nnz) {
   L.partials = take((size_t)(L.n_scan_partials + 1) * 4);
   L.partA = take((size_t)L.n_chunks * L.max_dim * 4);
   L.partB = take((size_t)L.n_chunks * L.max_dim * 4);
+  L.n_fold = (L.n_chunks + kFoldChunks - 1) / kFoldChunks;
+  L.partC = take((size_t)L.n_fold * L.max_dim * 4);   // folded partial of each block of kFoldChunks sub-chunks
+  L.folded = take((size_t)L.n_fold * 4);
   L.arow = take((size_t)L.n_chunks * 4);
   L.zero = take((size_t)EMB_MAX_DIM * 4);  // a zero grad_out row (the widest lane group) for positions that add nothing
   L.work = take(sizeof(unsigned));        // sub-chunk counter of the reduce
@@ -976,12 +982,30 @@ __global__ void __launch_bounds__(kRedWarps * 32, 8) segreduce_update_kernel(
     };
 
     unsigned prev_row = before;
+    // One-dim tables load each window's (row, bag) pairs while the previous
+    // window is walked (measured: 14.34 ms against 14.71 at 100M keys); on
+    // ragged tables the two extra registers spill and it loses (0.683 ms
+    // against 0.660), so they load at the window's start.
+    unsigned kk_n = 0, vv_n = 0;
+    if (kAllCols) {
+      kk_n = cs + li < ce ? K[cs + li] : kNoRow;
+      vv_n = cs + li < ce ? V[cs + li] : 0u;
+    }
     for (unsigned i0 = cs; i0 < ce; i0 += G) {
       // ---- lane-parallel bookkeeping, one position per lane
       const int m = (int)min((unsigned)G, ce - i0);
       const bool valid = li < m;
-      const unsigned kk = valid ? K[i0 + li] : kNoRow;
-      const unsigned vv = valid ? V[i0 + li] : 0u;
+      unsigned kk, vv;
+      if (kAllCols) {
+        kk = kk_n;
+        vv = vv_n;
+        const bool nx = i0 + G + li < ce;
+        kk_n = nx ? K[i0 + G + li] : kNoRow;
+        vv_n = nx ? V[i0 + G + li] : 0u;
+      } else {
+        kk = valid ? K[i0 + li] : kNoRow;
+        vv = valid ? V[i0 + li] : 0u;
+      }
       unsigned kp = __shfl_up_sync(gmask, kk, 1, G);
       const unsigned vp = __shfl_up_sync(gmask, vv, 1, G);
       if (li == 0) kp = prev_row;
@@ -1089,11 +1113,103 @@ __global__ void __launch_bounds__(kRedWarps * 32, 8) segreduce_update_kernel(
 // against 0.75 with 4 and 0.85 with 16.
 constexpr int kFixupLoads = 8;
 
+// Folds the partial rows of every block of kFoldChunks sub-chunks that lies
+// inside one row's run (the row began before the block and lasts through its
+// last position, so each of its sub-chunks left one partial of that row) into
+// one partial, summed in sub-chunk order by consecutive ranges per lane group
+// and a fixed xor tree; every other block is marked unfolded.  A row of
+// Zipf-head popularity spans thousands of sub-chunks: the fixup then adds
+// about 1/kFoldChunks as many partials for it.
+template <int G, int NCB>
+__global__ void __launch_bounds__(256) fold_kernel(TableView t, const unsigned* __restrict__ K, unsigned n,
+                                                   unsigned n_chunks, unsigned chunk, unsigned n_fold,
+                                                   const float* __restrict__ partB, float* __restrict__ partC,
+                                                   unsigned* __restrict__ folded) {
+  constexpr int P = 32 / G;
+  const int lane = threadIdx.x & 31;
+  const int sub = lane / G, li = lane % G;
+  const int maxd = t.max_dim;
+  const unsigned nwarps = (gridDim.x * blockDim.x) >> 5;
+  for (unsigned b = (blockIdx.x * blockDim.x + threadIdx.x) >> 5; b < n_fold; b += nwarps) {
+    const unsigned c0 = b * kFoldChunks;
+    bool fold = false;
+    unsigned row = 0;
+    if (c0 > 0 && c0 + kFoldChunks <= n_chunks) {
+      const size_t p0 = (size_t)c0 * chunk;
+      const size_t pe = (size_t)(c0 + kFoldChunks) * chunk;
+      const size_t p1 = (pe < (size_t)n ? pe : (size_t)n) - 1;
+      row = K[p0];
+      fold = row < t.n_rows && K[p0 - 1] == row && K[p1] == row;
+    }
+    if (lane == 0) folded[b] = fold ? 1u : 0u;
+    if (!fold) continue;
+    int D, col;
+    long long e0;
+    row_geom(t, row, D, col, e0);
+    constexpr unsigned per = (kFoldChunks + P - 1) / P;
+    const unsigned j0 = sub * per, j1 = min(kFoldChunks, j0 + per);
+    float acc[NCB][4], cmp[NCB][4];
+#pragma unroll
+    for (int cc = 0; cc < NCB; ++cc)
+#pragma unroll
+      for (int j = 0; j < 4; ++j) acc[cc][j] = cmp[cc][j] = 0.f;
+    constexpr int FB = kFixupLoads / NCB > 0 ? kFixupLoads / NCB : 1;
+    for (unsigned jb = j0; jb < j1; jb += FB) {
+      float4 x[FB][NCB];
+#pragma unroll
+      for (int q = 0; q < FB; ++q) {
+        const float* src = partB + (size_t)(c0 + jb + q) * maxd;
+#pragma unroll
+        for (int cc = 0; cc < NCB; ++cc) {
+          const int cidx = (cc * G + li) * 4;
+          x[q][cc] = (jb + q < j1 && cidx < D) ? *reinterpret_cast<const float4*>(src + cidx)
+                                               : make_float4(0.f, 0.f, 0.f, 0.f);
+        }
+      }
+#pragma unroll
+      for (int q = 0; q < FB; ++q) {
+        if (jb + q < j1) {
+#pragma unroll
+          for (int cc = 0; cc < NCB; ++cc) {
+            two_sum(acc[cc][0], cmp[cc][0], x[q][cc].x);
+            two_sum(acc[cc][1], cmp[cc][1], x[q][cc].y);
+            two_sum(acc[cc][2], cmp[cc][2], x[q][cc].z);
+            two_sum(acc[cc][3], cmp[cc][3], x[q][cc].w);
+          }
+        }
+      }
+    }
+#pragma unroll
+    for (int cc = 0; cc < NCB; ++cc)
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        for (int off = G; off < 32; off <<= 1) {
+          const float so = __shfl_xor_sync(0xffffffffu, acc[cc][j], off);
+          const float co = __shfl_xor_sync(0xffffffffu, cmp[cc][j], off);
+          two_sum(acc[cc][j], cmp[cc][j], so);
+          cmp[cc][j] = __fadd_rn(cmp[cc][j], co);
+        }
+        acc[cc][j] = __fadd_rn(acc[cc][j], cmp[cc][j]);
+      }
+    if (sub == 0) {
+      float* dst = partC + (size_t)b * maxd;
+#pragma unroll
+      for (int cc = 0; cc < NCB; ++cc) {
+        const int cidx = (cc * G + li) * 4;
+        if (cidx < D)
+          *reinterpret_cast<float4*>(dst + cidx) = make_float4(acc[cc][0], acc[cc][1], acc[cc][2], acc[cc][3]);
+      }
+    }
+  }
+}
+
 template <typename TW, int G, int NCB, typename Opt>
 __global__ void __launch_bounds__(256) fixup_kernel(TableView t, const unsigned* __restrict__ K, unsigned n,
                                                     unsigned n_chunks, unsigned chunk,
                                                     const float* __restrict__ partA,
                                                     const float* __restrict__ partB,
+                                                    const float* __restrict__ partC,
+                                                    const unsigned* __restrict__ folded,  // NULL: none folded
                                                     const unsigned* __restrict__ arow, Opt opt) {
   constexpr int P = 32 / G;
   const int lane = threadIdx.x & 31;
@@ -1121,33 +1237,52 @@ __global__ void __launch_bounds__(256) fixup_kernel(TableView t, const unsigned*
     int D, col;
     long long e0;
     row_geom(t, row, D, col, e0);
-    const unsigned m = c1 - c + 1;
-    const unsigned per = (m + P - 1) / P;
-    const unsigned j0 = sub * per, j1 = min(m, j0 + per);
+    // the P lane groups take consecutive ranges of the sub-chunks after the
+    // head, [c + 1, c1]; group 0 also takes the head partial.  Inside a
+    // group's range, a block of kFoldChunks sub-chunks that lies wholly in it
+    // and was folded contributes its one folded partial.
+    const unsigned span = c1 - c;
+    const unsigned per = (span + P - 1) / P;
+    const unsigned ga = min(c + 1 + sub * per, c1 + 1), gb = min(ga + per, c1 + 1);  // the group's [ga, gb)
     float acc[NCB][4], cmp[NCB][4];  // compensated (TwoSum) sums of the partial rows
 #pragma unroll
     for (int cc = 0; cc < NCB; ++cc)
 #pragma unroll
       for (int j = 0; j < 4; ++j) acc[cc][j] = cmp[cc][j] = 0.f;
     // partial rows are read kFixupLoads / NCB at a time (loads in flight per
-    // lane), then folded in in order
+    // lane), then added in order
     constexpr int FB = kFixupLoads / NCB > 0 ? kFixupLoads / NCB : 1;
-    for (unsigned jb = j0; jb < j1; jb += FB) {
+    bool head = sub == 0;
+    unsigned cp = ga;
+    while (head || cp < gb) {
       float4 x[FB][NCB];
+      unsigned have = 0;
 #pragma unroll
       for (int q = 0; q < FB; ++q) {
-        const unsigned j = jb + q;
-        const float* src = (j == 0 ? partA + (size_t)c * maxd : partB + (size_t)(c + j) * maxd);
+        const float* src = nullptr;
+        if (head) {
+          src = partA + (size_t)c * maxd;
+          head = false;
+        } else if (cp < gb) {
+          if (folded && cp % kFoldChunks == 0 && cp + kFoldChunks <= gb && folded[cp / kFoldChunks]) {
+            src = partC + (size_t)(cp / kFoldChunks) * maxd;
+            cp += kFoldChunks;
+          } else {
+            src = partB + (size_t)cp * maxd;
+            ++cp;
+          }
+        }
+        if (src) have |= 1u << q;
 #pragma unroll
         for (int cc = 0; cc < NCB; ++cc) {
           const int cidx = (cc * G + li) * 4;
-          x[q][cc] = (j < j1 && cidx < D) ? *reinterpret_cast<const float4*>(src + cidx)
-                                          : make_float4(0.f, 0.f, 0.f, 0.f);
+          x[q][cc] = (src && cidx < D) ? *reinterpret_cast<const float4*>(src + cidx)
+                                       : make_float4(0.f, 0.f, 0.f, 0.f);
         }
       }
 #pragma unroll
       for (int q = 0; q < FB; ++q) {
-        if (jb + q < j1) {
+        if ((have >> q) & 1u) {
 #pragma unroll
           for (int cc = 0; cc < NCB; ++cc) {
             two_sum(acc[cc][0], cmp[cc][0], x[q][cc].x);
@@ -1274,9 +1409,21 @@ static cudaError_t launch_reduce(const emb_table* t, const unsigned* K, const un
   // the fixup reads partial rows four columns per lane
   constexpr int G4 = G * VW / 4 > 32 ? 32 : G * VW / 4;
   constexpr int NCB4 = (G * VW * NCB) / (4 * G4);
+  // Rows that span whole blocks of kFoldChunks sub-chunks have those blocks
+  // folded first, so the fixup adds one partial per block (measured: fixup
+  // 0.63 -> 0.38 ms at 282M positions).  Below 2^24 positions no row is that
+  // long and the extra launch only costs time (0.005 ms at 4.5M to 6.5M).
+  float* pc = (float*)(ws + L.partC);
+  unsigned* fl = nullptr;
+  if ((size_t)n >= kFoldFrom) {
+    fl = (unsigned*)(ws + L.folded);
+    long long kblocks = std::min<long long>(((long long)L.n_fold * 32 + 255) / 256, resident_blocks(256));
+    fold_kernel<G4, NCB4><<<(int)std::max(1LL, kblocks), 256, 0, st>>>(v, K, n, L.n_chunks, L.chunk, L.n_fold, pb,
+                                                                       pc, fl);
+  }
   long long fblocks = std::min<long long>(((long long)L.n_chunks * 32 + 255) / 256, resident_blocks(256));
   fixup_kernel<TW, G4, NCB4, Opt><<<(int)std::max(1LL, fblocks), 256, 0, st>>>(v, K, n, L.n_chunks, L.chunk, pa,
-                                                                                   pb, ar, opt);
+                                                                                   pb, pc, fl, ar, opt);
   mark_phase(t, 3, st);
   return cudaGetLastError();
 }

@@ -19,7 +19,7 @@ exactly), which bounds the whole error by
 (3u for the roundings of each term: 1/L, its product with the count of a run
 of equal (row, bag) pairs, and the product with grad_out; 3u for a plain
 4-term group sum; u for the float32 partial of a row cut by a sub-chunk edge;
-DG_ULPS = 8 covers these 7u).  For keys with
+u for a folded block of such partials; DG_ULPS = 8 covers these 8u).  For keys with
 kappa > KAPPA the gates add that bound propagated through the update:
   accumulator  + 2 |g| dg + dg^2         (acc' = acc + g^2)
   weight       + lr * dg / sqrt(acc')    (|d/dg (g / sqrt(acc + g^2))| <= 1/sqrt(acc'))

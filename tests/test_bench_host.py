@@ -30,11 +30,14 @@ def test_fingerprint_is_stable():
 
 
 def test_launches_per_step_follow_the_digit_width():
-    # placement (6) + recording forward, 5 launches per radix pass, reduce, fixup;
-    # the backward sorts rows within a slot: the largest slot's key count sets the passes
-    assert bench.launches_per_step(1_562_500, E.EMB_SORT_DIGIT_BITS) == 7 + 3 * 5 + 2     # 21 bits, 3 passes
+    # placement (6) + recording forward, 5 launches per radix pass, reduce, fixup, and from
+    # 2^24 lookups the fold kernel; the backward sorts rows within a slot: the largest
+    # slot's key count sets the passes
+    big = 1 << 24
+    assert bench.launches_per_step(1_562_500, E.EMB_SORT_DIGIT_BITS, nnz=big) == 7 + 3 * 5 + 3   # 21 bits, 3 passes
+    assert bench.launches_per_step(1_562_500, E.EMB_SORT_DIGIT_BITS, nnz=big - 1) == 7 + 3 * 5 + 2
     assert bench.launches_per_step(16_383, E.EMB_SORT_DIGIT_BITS) == 7 + 2 * 5 + 2        # 14 bits, 2 passes
     assert bench.launches_per_step(16_384, E.EMB_SORT_DIGIT_BITS) == 7 + 3 * 5 + 2        # 15 bits, 3 passes
     assert bench.launches_per_step(100, 7) == 7 + 1 * 5 + 2
     # the dedupe forward: placement, expand, the sort, dedupe pooling; the backward skips its sort
-    assert bench.launches_per_step(1_562_500, E.EMB_SORT_DIGIT_BITS, dedup=True) == 7 + 3 * 5 + 1 + 2
+    assert bench.launches_per_step(1_562_500, E.EMB_SORT_DIGIT_BITS, dedup=True, nnz=big) == 7 + 3 * 5 + 1 + 3
