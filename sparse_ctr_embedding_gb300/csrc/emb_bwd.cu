@@ -340,8 +340,7 @@ __global__ void __launch_bounds__(kSortThreads, 3) radix_scatter_kernel(
   unsigned(*cnt)[kDigits] = reinterpret_cast<unsigned(*)[kDigits]>(smem);  // [kSortWarps][kDigits]
   unsigned* gbase = smem + kSortWarps * kDigits;                             // [kDigits]
   unsigned* wtot = gbase + kDigits;                                           // [33]
-  unsigned* tk = wtot + 33;                                                   // [kSortTile]
-  unsigned* tv = tk + kSortTile;                                              // [kSortTile]
+  uint2* tkv = reinterpret_cast<uint2*>(wtot + 34);                          // [kSortTile] (8-byte aligned)
   __shared__ unsigned reg;
   const int w = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const unsigned tile = blockIdx.x;
@@ -406,18 +405,18 @@ __global__ void __launch_bounds__(kSortThreads, 3) radix_scatter_kernel(
   for (int q = 0; q < kSortItems; ++q) {
     if (valid[q]) {
       const unsigned pos = cnt[w][d[q]] + rank[q];
-      tk[pos] = k[q];
-      tv[pos] = v[q];
+      tkv[pos] = make_uint2(k[q], v[q]);
     }
   }
   __syncthreads();
   const unsigned tile_n = hi - lo;
   for (unsigned j = threadIdx.x; j < tile_n; j += kSortThreads) {
-    const unsigned kk = tk[j];
+    const uint2 kv = tkv[j];
+    const unsigned kk = kv.x;
     const unsigned dg = region_digit(g, kk, shift);
     const unsigned gp = gbase[dg] + j;
     kout[gp] = kk;
-    vout[gp] = tv[j];
+    vout[gp] = kv.y;
   }
 }
 
@@ -1366,7 +1365,7 @@ cudaError_t launch_scan_u32(const unsigned* in, unsigned* out, size_t n, unsigne
 }
 
 static size_t scatter_smem() {
-  return sizeof(unsigned) * ((size_t)kSortWarps * kDigits + kDigits + 33 + 2 * (size_t)kSortTile);
+  return sizeof(unsigned) * ((size_t)kSortWarps * kDigits + kDigits + 34 + 2 * (size_t)kSortTile);
 }
 
 // Record the caller's timing event for a finished backward phase, if any.
