@@ -54,8 +54,32 @@ def parse():
     return ap.parse_args()
 
 
+def strip_comments(src: str) -> str:
+    """C/C++ source without its comments and blank lines (string and character literals kept)."""
+    out, i, n = [], 0, len(src)
+    while i < n:
+        c = src[i]
+        if c in "\"'":
+            j = i + 1
+            while j < n and src[j] != c:
+                j += 2 if src[j] == "\\" else 1
+            out.append(src[i:j + 1])
+            i = j + 1
+        elif src.startswith("//", i):
+            j = src.find("\n", i)
+            i = n if j < 0 else j
+        elif src.startswith("/*", i):
+            j = src.find("*/", i + 2)
+            i = n if j < 0 else j + 2
+        else:
+            out.append(c)
+            i += 1
+    return "\n".join(line.rstrip() for line in "".join(out).splitlines() if line.strip())
+
+
 def kernel_fingerprint() -> str:
-    """sha256 of the CUDA sources and the C ABI header: ties a stored ncu figure to the code it measured."""
+    """sha256 of the CUDA sources and the C ABI header with comments removed: ties a stored ncu
+    figure to the code it measured (an edit of comments alone keeps it)."""
     import hashlib
 
     h = hashlib.sha256()
@@ -63,8 +87,8 @@ def kernel_fingerprint() -> str:
     files = sorted(os.path.join(csrc, f) for f in os.listdir(csrc) if f.endswith((".cu", ".cuh")))
     for f in files + [os.path.join(ROOT, "include", "emb_gb300.h")]:
         h.update(os.path.basename(f).encode())
-        with open(f, "rb") as fh:
-            h.update(fh.read())
+        with open(f, encoding="utf-8") as fh:
+            h.update(strip_comments(fh.read()).encode())
     return h.hexdigest()
 
 

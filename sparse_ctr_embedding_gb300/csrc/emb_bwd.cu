@@ -1,38 +1,48 @@
-// Backward: duplicate-key gradient reduction + element-wise sparse Adagrad.
+// Backward: duplicate-key gradient reduction + the fused sparse update
+// (element-wise Adagrad, or FTRL-Proximal).
 //
 // Tencent PCG DataFun talk, "计算优化": one backward kernel updates every
 // feature of the unified table.  JD ads article, 3.2.1: Adagrad keeps a
 // per-parameter sum of squared gradients, updates element-wise, and leaves
-// features that are absent from the batch untouched.
+// features that are absent from the batch untouched; FTRL is the other
+// sparse optimizer it names.
 //
 // Pipeline (all on the caller's stream, no host synchronisation):
-//  1. expand    one warp per bag: probe each key; emit the pair
-//               (internal row, bag) per occurrence (row = n_rows for a miss,
-//               which sorts last) and, for mean, 1/L per bag.
-//  2. sort      stable LSD radix sort of the pairs by row (hand-written:
-//               per-tile digit counts, a device-wide scan, then a stable
-//               scatter ranked with warp match/ballot and staged in shared
-//               memory so every digit run is written contiguously).
-//               Rows are numbered slot-major, so the sorted order walks one
-//               feature slot (one column block of grad_out) at a time.
-//  3. reduce    the sorted positions are cut into sub-chunks (256 positions,
-//               fewer for small batches); one warp
-//               per chunk.  Every run of equal rows inside a chunk ("piece")
-//               is summed in float32 with TwoSum compensation, in sorted
-//               order (so in occurrence order: the sort is stable), by a
-//               group of G lanes.  A piece
-//               that is a whole segment (all occurrences of its row) applies
-//               Adagrad to the row directly.  A piece cut by a chunk edge
-//               leaves a partial sum: the head piece of a segment in slot A
-//               of its chunk, later pieces in slot B of theirs.
-//  4. fixup     one warp per segment that spans chunks: A + B + B ... in
-//               chunk order (compensated, then a fixed tree across the
-//               warp's lane groups), then Adagrad.
+//  0. placement the bag lengths, transposed to slot-major order and scanned,
+//               give every bag's first pair position: each slot's pairs
+//               form one region of the pair arrays.
+//  1. expand    (without a recording forward) one warp per bag: probe each
+//               key; write the pair (internal row, bag) of every occurrence
+//               at its placed position (row = n_rows for a miss, which sorts
+//               last in its slot) and, for mean, 1/L per bag.
+//  2. sort      stable LSD radix sort of each region's pairs by the in-slot
+//               row number (hand-written: per-tile digit counts, a
+//               device-wide scan, then a stable scatter ranked with warp
+//               match and staged in shared memory so every digit run is
+//               written contiguously).  Rows are numbered slot-major, so the
+//               sorted order walks one feature slot (one column block of
+//               grad_out) at a time.
+//  3. reduce    the sorted positions are cut into sub-chunks (128 or 256
+//               positions, fewer for small batches) taken in order from a
+//               counter by groups of G lanes.  Every run of equal rows
+//               inside a sub-chunk ("piece") is summed in float32 with TwoSum
+//               compensation, in sorted order (so in occurrence order: the
+//               sort is stable).  A piece that is a whole segment (all
+//               occurrences of its row) gets the update directly.  A piece
+//               cut by a sub-chunk edge leaves a partial sum: the head piece
+//               of a segment in slot A of its sub-chunk, later pieces in
+//               slot B of theirs.
+//  4. fold      (large batches) every block of 32 sub-chunks inside one
+//               row's run has its slot-B partials summed into one.
+//  5. fixup     one warp per segment that spans sub-chunks: A + B + B ...
+//               (a folded block as one) in sub-chunk order (compensated,
+//               then a fixed tree across the warp's lane groups), then the
+//               update.
 // No float atomics: every sum has a fixed order, so the step is bitwise
 // reproducible.  The Adagrad arithmetic per element, in float32:
 //   g = G;  acc += g * g;  w -= lr * g / (sqrt(acc) + eps)
 // with sqrt and the quotient from the hardware reciprocal square root and
-// reciprocal (a few ulp; see adagrad_elem), half weights rounded to
+// fast division (a few ulp; see AdagradStep), half weights rounded to
 // nearest-even on store.
 #include <algorithm>
 #include <cstdio>

@@ -29,6 +29,14 @@ def test_fingerprint_is_stable():
     assert len(fp) == 64 and fp == bench.kernel_fingerprint()
 
 
+def test_fingerprint_ignores_comments_only():
+    a = 'int f(int x) { return x + 1; }  // one\n/* two */\nconst char* s = "//not a comment";\n'
+    b = '// header\nint f(int x) { return x + 1; }\n\nconst char* s = "//not a comment";  /* tail */\n'
+    assert bench.strip_comments(a) == bench.strip_comments(b)
+    assert "//not a comment" in bench.strip_comments(a)
+    assert bench.strip_comments(a) != bench.strip_comments(a.replace("x + 1", "x + 2"))
+
+
 def test_launches_per_step_follow_the_digit_width():
     # placement (6) + recording forward, 5 launches per radix pass, reduce, fixup, and from
     # 2^24 lookups the fold kernel; the backward sorts rows within a slot: the largest
