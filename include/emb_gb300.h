@@ -276,9 +276,11 @@ EMB_API emb_status emb_bwd_ftrl(emb_table* table, const int64_t* offsets_d, int6
  * emb_bwd_phase_events -- optional timing hook (no counterpart in the pages;
  * it serves measurement).  Registers up to EMB_BWD_PHASES caller-owned
  * cudaEvent_t handles (passed as void*, created with timing enabled) that
- * every later emb_bwd_adagrad call on this table records, on its stream,
- * after each of its phases: [0] expand (probe to row/bag pairs), [1] radix
- * sort, [2] segmented reduce + Adagrad, [3] cross-chunk fixup.  Elapsed times
+ * every later backward call on this table (emb_bwd_adagrad, emb_bwd_ftrl and
+ * their recorded and no-alloc forms) records, on its stream, after each of
+ * its phases: [0] expand (probe to row/bag pairs; nothing after a recording
+ * forward), [1] radix sort, [2] segmented reduce + update, [3] the fold of
+ * long rows' partials (large batches) and the cross-chunk fixup.  Elapsed times
  * between an event recorded just before the call and these give each
  * phase's device time.  n = 0 removes the hook.  The events must outlive
  * the calls that record them.
