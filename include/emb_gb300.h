@@ -441,15 +441,17 @@ EMB_API emb_status emb_check_device_flag(emb_table* table, void* stream, uint32_
  *                          pipeline uploads gradients) into a free set on the
  *                          upload stream; returns a ticket (0, 1, 2, ...).
  *                          It may run ahead of the step by up to depth - 1
- *                          batches: that is the overlap.  A set is reused
- *                          only after its previous batch's backward and
- *                          download are done (the upload stream waits on the
+ *                          batches: that is the overlap.  A set's inputs are
+ *                          overwritten only after its previous batch's
+ *                          backward is done (the upload stream waits on the
  *                          GPU; the host does not block).
  *   emb_pipeline_forward   the recording forward of that batch on the compute
- *                          stream, after its upload; pooled output into out_d
+ *                          stream, after its upload and after the download of
+ *                          the set's previous batch; pooled output into out_d
  *                          (or, NULL, the set's own buffer, returned through
  *                          out_used) and, if out_h is given, copied to out_h
- *                          on the download stream.
+ *                          on the download stream.  A caller's out_d must not
+ *                          be written again before that copy is done.
  *   emb_pipeline_backward_adagrad / _ftrl
  *                          the recorded backward of that batch with grad_out_d
  *                          (device) or, NULL, the uploaded grad_out; then the

@@ -15,10 +15,13 @@
 // pipeline does not do.
 //
 // Each in-flight batch owns one of `depth` buffer sets (CSR offsets and
-// keys, optionally grad_out, the pooled output, the backward workspace); a
-// set is handed to batch t only after batch t - depth has finished its
-// backward and its download, which the upload stream waits for on the GPU
-// (events), so the host never blocks except in emb_pipeline_wait.
+// keys, optionally grad_out, the pooled output, the backward workspace).
+// Batch t's upload into a set waits only for batch t - depth's backward (the
+// last reader of the set's inputs), and batch t's forward, which writes the
+// set's pooled output, waits for batch t - depth's download of it: the
+// download of one batch never holds up the upload of a later one.  All
+// waits are GPU-side (events), so the host never blocks except in
+// emb_pipeline_wait.
 #include <algorithm>
 #include <vector>
 
@@ -36,7 +39,8 @@ struct PipeSet {
   cudaEvent_t uploaded = nullptr;   // the batch's inputs are on the device
   cudaEvent_t forwarded = nullptr;  // the forward wrote `out`
   cudaEvent_t bwd_done = nullptr;   // the backward (or, forward-only, the forward) finished
-  cudaEvent_t released = nullptr;   // backward and download done: the set may be reused
+  cudaEvent_t downloaded = nullptr; // the download stream passed the batch's pooled-output copy
+  cudaEvent_t released = nullptr;   // backward and download done (emb_pipeline_wait)
   long long ticket = -1;
   long long n_bags = 0, nnz = 0;
   int pool = 0;
@@ -73,6 +77,7 @@ static void pipe_free(emb_pipeline* p) {
     if (s.uploaded) cudaEventDestroy(s.uploaded);
     if (s.forwarded) cudaEventDestroy(s.forwarded);
     if (s.bwd_done) cudaEventDestroy(s.bwd_done);
+    if (s.downloaded) cudaEventDestroy(s.downloaded);
     if (s.released) cudaEventDestroy(s.released);
   }
   if (p->up) cudaStreamDestroy(p->up);
@@ -126,8 +131,12 @@ emb_status emb_pipeline_create(emb_table* table, int64_t max_bags, int64_t max_n
       EMB_CUDA(cudaEventCreateWithFlags(&s.uploaded, cudaEventDisableTiming));
       EMB_CUDA(cudaEventCreateWithFlags(&s.forwarded, cudaEventDisableTiming));
       EMB_CUDA(cudaEventCreateWithFlags(&s.bwd_done, cudaEventDisableTiming));
+      EMB_CUDA(cudaEventCreateWithFlags(&s.downloaded, cudaEventDisableTiming));
       EMB_CUDA(cudaEventCreateWithFlags(&s.released, cudaEventDisableTiming));
-      EMB_CUDA(cudaEventRecord(s.released, p->up));  // every set starts free
+      // every set starts free
+      EMB_CUDA(cudaEventRecord(s.bwd_done, p->up));
+      EMB_CUDA(cudaEventRecord(s.downloaded, p->up));
+      EMB_CUDA(cudaEventRecord(s.released, p->up));
     }
     return EMB_OK;
   };
@@ -158,8 +167,8 @@ emb_status emb_pipeline_submit(emb_pipeline* p, const int64_t* offsets_h, int64_
   PipeSet& s = p->sets[(size_t)(t % p->depth)];
   if (s.state == PipeSet::kSubmitted || s.state == PipeSet::kForwarded)
     return fail(EMB_ERR_INVALID_ARG, "the buffer set is still held by a batch whose backward (or release) has not been called");
-  // the set's previous batch must have finished its backward and download
-  EMB_CUDA(cudaStreamWaitEvent(p->up, s.released, 0));
+  // the set's previous batch must have finished its backward (the last reader of the inputs)
+  EMB_CUDA(cudaStreamWaitEvent(p->up, s.bwd_done, 0));
   EMB_CUDA(cudaMemcpyAsync(s.offsets, offsets_h, (size_t)(n_bags + 1) * 8, cudaMemcpyHostToDevice, p->up));
   if (nnz > 0) EMB_CUDA(cudaMemcpyAsync(s.keys, keys_h, (size_t)nnz * 8, cudaMemcpyHostToDevice, p->up));
   if (grad_out_h) {
@@ -184,6 +193,8 @@ emb_status emb_pipeline_forward(emb_pipeline* p, int64_t ticket, emb_pool pool, 
   if (!s || s->state != PipeSet::kSubmitted) return fail(EMB_ERR_INVALID_ARG, "unknown ticket, or its forward already ran");
   float* out = out_d ? out_d : s->out;
   EMB_CUDA(cudaStreamWaitEvent(p->compute, s->uploaded, 0));
+  // the set's previous batch's pooled output must have been copied out
+  EMB_CUDA(cudaStreamWaitEvent(p->compute, s->downloaded, 0));
   emb_status rc = emb_lookup_fwd_record(p->table, s->offsets, s->n_bags, s->keys, s->nnz, pool, out, s->ws,
                                         s->ws_bytes, p->compute);
   if (rc != EMB_OK) return rc;
@@ -192,6 +203,7 @@ emb_status emb_pipeline_forward(emb_pipeline* p, int64_t ticket, emb_pool pool, 
     const size_t bytes = (size_t)(s->n_bags / p->table->st.n_slots) * (size_t)p->table->st.sum_dims * 4;
     EMB_CUDA(cudaStreamWaitEvent(p->down, s->forwarded, 0));
     if (bytes) EMB_CUDA(cudaMemcpyAsync(out_h, out, bytes, cudaMemcpyDeviceToHost, p->down));
+    EMB_CUDA(cudaEventRecord(s->downloaded, p->down));
   }
   s->pool = (int)pool;
   s->state = PipeSet::kForwarded;
