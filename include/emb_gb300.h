@@ -454,8 +454,10 @@ EMB_API emb_status emb_check_device_flag(emb_table* table, void* stream, uint32_
  *                          be written again before that copy is done.
  *   emb_pipeline_backward_adagrad / _ftrl
  *                          the recorded backward of that batch with grad_out_d
- *                          (device) or, NULL, the uploaded grad_out; then the
- *                          set is released.  Must come before the next
+ *                          (device) or, NULL, the uploaded grad_out (uploaded
+ *                          after the CSR batch, so the forward does not wait
+ *                          for it; the backward does); then the set is
+ *                          released.  Must come before the next
  *                          batch's forward (the table keeps one recording).
  *   emb_pipeline_release   instead of a backward: release a forwarded set
  *                          (forward-only use).

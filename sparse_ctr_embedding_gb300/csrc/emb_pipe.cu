@@ -36,7 +36,8 @@ struct PipeSet {
   float* out = nullptr;          // device f32[max_batch * sum_dims]
   void* ws = nullptr;            // backward workspace
   size_t ws_bytes = 0;
-  cudaEvent_t uploaded = nullptr;   // the batch's inputs are on the device
+  cudaEvent_t uploaded = nullptr;   // the batch's CSR offsets and keys are on the device
+  cudaEvent_t grad_up = nullptr;    // and its grad_out (uploaded after them: only the backward needs it)
   cudaEvent_t forwarded = nullptr;  // the forward wrote `out`
   cudaEvent_t bwd_done = nullptr;   // the backward (or, forward-only, the forward) finished
   cudaEvent_t downloaded = nullptr; // the download stream passed the batch's pooled-output copy
@@ -75,6 +76,7 @@ static void pipe_free(emb_pipeline* p) {
     dfree(s.out);
     dfree(s.ws);
     if (s.uploaded) cudaEventDestroy(s.uploaded);
+    if (s.grad_up) cudaEventDestroy(s.grad_up);
     if (s.forwarded) cudaEventDestroy(s.forwarded);
     if (s.bwd_done) cudaEventDestroy(s.bwd_done);
     if (s.downloaded) cudaEventDestroy(s.downloaded);
@@ -129,6 +131,7 @@ emb_status emb_pipeline_create(emb_table* table, int64_t max_bags, int64_t max_n
       EMB_CUDA(dmalloc(&s.ws, ws_bytes));
       s.ws_bytes = ws_bytes;
       EMB_CUDA(cudaEventCreateWithFlags(&s.uploaded, cudaEventDisableTiming));
+      EMB_CUDA(cudaEventCreateWithFlags(&s.grad_up, cudaEventDisableTiming));
       EMB_CUDA(cudaEventCreateWithFlags(&s.forwarded, cudaEventDisableTiming));
       EMB_CUDA(cudaEventCreateWithFlags(&s.bwd_done, cudaEventDisableTiming));
       EMB_CUDA(cudaEventCreateWithFlags(&s.downloaded, cudaEventDisableTiming));
@@ -171,11 +174,13 @@ emb_status emb_pipeline_submit(emb_pipeline* p, const int64_t* offsets_h, int64_
   EMB_CUDA(cudaStreamWaitEvent(p->up, s.bwd_done, 0));
   EMB_CUDA(cudaMemcpyAsync(s.offsets, offsets_h, (size_t)(n_bags + 1) * 8, cudaMemcpyHostToDevice, p->up));
   if (nnz > 0) EMB_CUDA(cudaMemcpyAsync(s.keys, keys_h, (size_t)nnz * 8, cudaMemcpyHostToDevice, p->up));
+  EMB_CUDA(cudaEventRecord(s.uploaded, p->up));
+  // grad_out last: the forward can start as soon as the CSR batch is in
   if (grad_out_h) {
     const size_t bytes = (size_t)(n_bags / p->table->st.n_slots) * (size_t)p->table->st.sum_dims * 4;
     if (bytes) EMB_CUDA(cudaMemcpyAsync(s.grad, grad_out_h, bytes, cudaMemcpyHostToDevice, p->up));
   }
-  EMB_CUDA(cudaEventRecord(s.uploaded, p->up));
+  EMB_CUDA(cudaEventRecord(s.grad_up, p->up));
   s.ticket = t;
   s.n_bags = n_bags;
   s.nnz = nnz;
@@ -229,6 +234,7 @@ static emb_status pipe_backward(emb_pipeline* p, int64_t ticket, const float* gr
   if (!s || s->state != PipeSet::kForwarded) return fail(EMB_ERR_INVALID_ARG, "unknown ticket, or its forward has not run");
   const float* g = grad_out_d ? grad_out_d : (s->has_grad ? s->grad : nullptr);
   if (!g && s->n_bags > 0) return fail(EMB_ERR_INVALID_ARG, "no grad_out: pass one or upload it with the batch");
+  if (!grad_out_d && s->has_grad) EMB_CUDA(cudaStreamWaitEvent(p->compute, s->grad_up, 0));
   emb_status rc = ftrl ? emb_bwd_ftrl_recorded(p->table, s->n_bags, s->nnz, (emb_pool)s->pool, g, fp, s->ws,
                                                s->ws_bytes, p->compute)
                        : emb_bwd_adagrad_recorded(p->table, s->n_bags, s->nnz, (emb_pool)s->pool, g, lr, eps, s->ws,
