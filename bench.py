@@ -77,14 +77,21 @@ def strip_comments(src: str) -> str:
     return "\n".join(line.rstrip() for line in "".join(out).splitlines() if line.strip())
 
 
+# The sources of the step's kernels and of the table they read (the forward, the
+# backward, the host table build and the shared device code): a stored ncu figure
+# is tied to these.  The batch pipeline and the device table build are host-side
+# orchestration the captured kernels do not depend on.
+STEP_SOURCES = ("emb_bwd.cu", "emb_fwd.cu", "emb_internal.cuh", "emb_table.cu")
+
+
 def kernel_fingerprint() -> str:
-    """sha256 of the CUDA sources and the C ABI header with comments removed: ties a stored ncu
-    figure to the code it measured (an edit of comments alone keeps it)."""
+    """sha256 of the step kernels' sources and the C ABI header with comments removed: ties a
+    stored ncu figure to the code it measured (an edit of comments alone keeps it)."""
     import hashlib
 
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "sparse_ctr_embedding_gb300", "csrc")
-    files = sorted(os.path.join(csrc, f) for f in os.listdir(csrc) if f.endswith((".cu", ".cuh")))
+    files = [os.path.join(csrc, f) for f in STEP_SOURCES]
     for f in files + [os.path.join(ROOT, "include", "emb_gb300.h")]:
         h.update(os.path.basename(f).encode())
         with open(f, encoding="utf-8") as fh:
