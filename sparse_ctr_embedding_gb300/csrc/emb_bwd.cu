@@ -488,18 +488,38 @@ __global__ void __launch_bounds__(kScanThreads) scan_down_kernel(const unsigned*
   __shared__ unsigned wt[33];
   // blocked arrangement: thread t owns kScanItems consecutive elements
   const size_t base = (size_t)blockIdx.x * kScanTile + (size_t)threadIdx.x * kScanItems;
+  // a whole run of kScanItems in range moves as 16-byte vectors (in and out
+  // are 16-byte aligned and base is a multiple of 16 elements)
+  const bool whole = base + kScanItems <= n;
   unsigned v[kScanItems];
   unsigned s = 0;
+  if (whole) {
 #pragma unroll
-  for (int j = 0; j < kScanItems; ++j) {
-    v[j] = base + j < n ? in[base + j] : 0;
-    s += v[j];
+    for (int j = 0; j < kScanItems; j += 4) {
+      const uint4 x = *reinterpret_cast<const uint4*>(in + base + j);
+      v[j] = x.x; v[j + 1] = x.y; v[j + 2] = x.z; v[j + 3] = x.w;
+    }
+  } else {
+#pragma unroll
+    for (int j = 0; j < kScanItems; ++j) v[j] = base + j < n ? in[base + j] : 0;
   }
+#pragma unroll
+  for (int j = 0; j < kScanItems; ++j) s += v[j];
   unsigned excl = block_excl_scan(s, wt) + partials[blockIdx.x];
+  unsigned o[kScanItems];
 #pragma unroll
   for (int j = 0; j < kScanItems; ++j) {
-    if (base + j < n) out[base + j] = excl;
+    o[j] = excl;
     excl += v[j];
+  }
+  if (whole) {
+#pragma unroll
+    for (int j = 0; j < kScanItems; j += 4)
+      *reinterpret_cast<uint4*>(out + base + j) = make_uint4(o[j], o[j + 1], o[j + 2], o[j + 3]);
+  } else {
+#pragma unroll
+    for (int j = 0; j < kScanItems; ++j)
+      if (base + j < n) out[base + j] = o[j];
   }
 }
 
