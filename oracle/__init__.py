@@ -62,6 +62,8 @@ def lib():
         L.orc_grad_free.restype = None
         L.orc_adagrad.argtypes = [_vp, ctypes.c_int64, ctypes.c_int, _vp, _vp, ctypes.c_float, ctypes.c_float]
         L.orc_f32_to_f16.argtypes = [_vp, ctypes.c_int64, _vp]
+        L.orc_rowwise_adagrad.argtypes = [_vp, _vp, ctypes.c_int64, ctypes.c_int, _vp, _vp, ctypes.c_float,
+                                          ctypes.c_float]
         L.orc_ftrl.argtypes = [_vp, ctypes.c_int64, ctypes.c_int, _vp, _vp, _vp, ctypes.c_float, ctypes.c_float,
                                ctypes.c_float, ctypes.c_float]
         _lib = L
@@ -201,6 +203,23 @@ def adagrad(G: np.ndarray, w: np.ndarray, acc: np.ndarray, lr: float, eps: float
         w = w.astype(np.float32)
     assert G.size == w.size == acc.size
     _check(lib().orc_adagrad(_p(G), G.size, wd, _p(w), _p(acc), ctypes.c_float(lr), ctypes.c_float(eps)))
+    return w, acc
+
+
+def rowwise_adagrad(G: np.ndarray, goff: np.ndarray, w: np.ndarray, acc_rows: np.ndarray, lr: float,
+                    eps: float) -> Tuple[np.ndarray, np.ndarray]:
+    """Row-wise Adagrad on copies of (w, acc_rows): rows r = G[goff[r]:goff[r+1]], one
+    accumulator per row; w float32 or float16.  Returns (w', acc_rows')."""
+    G = np.ascontiguousarray(G, dtype=np.float64)
+    goff = np.ascontiguousarray(goff, dtype=np.int64)
+    w = np.array(w, copy=True)
+    acc = np.array(acc_rows, dtype=np.float32, copy=True)
+    wd = 1 if w.dtype == np.float16 else 0
+    if wd == 0:
+        w = w.astype(np.float32)
+    assert G.size == w.size == goff[-1] and acc.size == goff.size - 1
+    _check(lib().orc_rowwise_adagrad(_p(G), _p(goff), acc.size, wd, _p(w), _p(acc), ctypes.c_float(lr),
+                                     ctypes.c_float(eps)))
     return w, acc
 
 

@@ -344,6 +344,40 @@ int orc_adagrad(const double* G, int64_t n, int wdtype, void* w, float* acc, flo
   return ORC_OK;
 }
 
+// Row-wise Adagrad: Adagrad ([JD] 3.2.1) with one accumulator per row instead
+// of one per element.  The pages give no formula for this variant; the
+// reading here adds the mean of the row's squared gradient.  Per row r of D
+// elements (rows given by goff), in float32 and this order:
+//   g_d = (float)G_d;  s = sum_d g_d*g_d (d ascending);  m = s / D;
+//   a = acc[r] + m;  den = sqrt(a) + eps;  w_d = w_d - (lr*g_d)/den.
+// Half weights are read exactly and the result rounded to half (RNE).
+int orc_rowwise_adagrad(const double* G, const int64_t* goff, int64_t n_rows, int wdtype, void* w, float* acc,
+                        float lr, float eps) {
+  for (int64_t r = 0; r < n_rows; ++r) {
+    const int64_t b = goff[r], e = goff[r + 1];
+    if (e <= b) continue;
+    float s = 0.f;
+    for (int64_t i = b; i < e; ++i) {
+      const float g = (float)G[i];
+      s = s + g * g;
+    }
+    const float m = s / (float)(e - b);
+    const float a = acc[r] + m;
+    const float den = std::sqrt(a) + eps;
+    acc[r] = a;
+    for (int64_t i = b; i < e; ++i) {
+      const float g = (float)G[i];
+      const float wv = (wdtype == 1) ? (float)((_Float16*)w)[i] : ((float*)w)[i];
+      const float nw = wv - (lr * g) / den;
+      if (wdtype == 1)
+        ((_Float16*)w)[i] = (_Float16)nw;
+      else
+        ((float*)w)[i] = nw;
+    }
+  }
+  return ORC_OK;
+}
+
 // FTRL-Proximal, per coordinate (McMahan et al., "Ad Click Prediction: a View
 // from the Trenches", KDD 2013, Algorithm 1; the JD article 3.2.1 names FTRL as
 // the other sparse optimizer of CTR training).  For each element, with the

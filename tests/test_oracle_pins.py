@@ -20,6 +20,69 @@ GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
 M64 = (1 << 64) - 1
 
 
+# ------------------------------------------------------------------ row-wise Adagrad
+
+def _torch_adagrad(w0, G, acc0, lr, eps):
+    p = torch.nn.Parameter(torch.from_numpy(np.asarray(w0, dtype=np.float32).copy()))
+    opt = torch.optim.Adagrad([p], lr=lr, eps=eps, initial_accumulator_value=float(acc0))
+    p.grad = torch.from_numpy(np.asarray(G, dtype=np.float32))
+    opt.step()
+    return p.detach().numpy(), opt.state[p]["sum"].numpy()
+
+
+def test_rowwise_adagrad_one_element_rows_match_torch_adagrad():
+    # a row of one element: the row-wise rule is element-wise Adagrad (the library routine)
+    rng = np.random.default_rng(31)
+    n = 2048
+    w0 = rng.uniform(-0.05, 0.05, n).astype(np.float32)
+    G = rng.standard_normal(n) * rng.choice([1e-3, 1.0, 30.0], size=n)
+    w, acc = oracle.rowwise_adagrad(G, np.arange(n + 1), w0, np.full(n, 0.1, np.float32), 0.01, 1e-8)
+    ref_w, ref_acc = _torch_adagrad(w0, G, 0.1, 0.01, 1e-8)
+    np.testing.assert_allclose(acc, ref_acc, rtol=2 ** -23, atol=0)
+    np.testing.assert_allclose(w, ref_w, rtol=0, atol=2 * np.spacing(np.abs(ref_w)).max())
+
+
+def test_rowwise_adagrad_equal_gradients_match_elementwise_adagrad():
+    # every element of a row with the same gradient g: the row's mean square is g^2, so each
+    # element follows torch's element-wise Adagrad from the row's accumulator
+    rng = np.random.default_rng(32)
+    dims = rng.integers(1, 65, 300)
+    goff = np.concatenate([[0], np.cumsum(dims)])
+    g_row = rng.standard_normal(dims.size) * 0.5
+    G = np.repeat(g_row, dims)
+    w0 = rng.uniform(-0.05, 0.05, int(goff[-1])).astype(np.float32)
+    w, acc = oracle.rowwise_adagrad(G, goff, w0, np.full(dims.size, 0.1, np.float32), 0.05, 1e-8)
+    ref_w, ref_acc = _torch_adagrad(w0, G, 0.1, 0.05, 1e-8)
+    # the float32 sum of D equal squares carries up to about D roundings of g^2
+    u = 2.0 ** -24
+    a_tol = (dims + 2) * u
+    np.testing.assert_array_less(np.abs(acc - ref_acc[goff[:-1]]), a_tol * ref_acc[goff[:-1]] + 1e-30)
+    step = np.abs(0.05 * G / np.sqrt(np.repeat(ref_acc[goff[:-1]], dims)))
+    w_tol = np.repeat(a_tol, dims) * step + 2 * np.spacing(np.abs(ref_w))
+    np.testing.assert_array_less(np.abs(w - ref_w), w_tol)
+
+
+def test_rowwise_adagrad_worked_example_and_order_invariance():
+    # hand-worked: g = (1, 7), mean square 25, accumulator 0 -> 25, sqrt 5; lr 5, eps 0:
+    # each weight moves by exactly its gradient
+    w, acc = oracle.rowwise_adagrad(np.array([1.0, 7.0]), np.array([0, 2]), np.array([10.0, 20.0], np.float32),
+                                    np.array([0.0], np.float32), 5.0, 0.0)
+    assert np.array_equal(w, np.array([9.0, 13.0], np.float32)) and np.array_equal(acc, np.array([25.0], np.float32))
+    # two rows: permuting a row's elements permutes its results (integer gradients: exact sums)
+    G = np.array([3.0, -4.0, 12.0, 1.0, 2.0])
+    goff = np.array([0, 3, 5])
+    w0 = np.array([1.0, 2.0, 3.0, 4.0, 5.0], np.float32)
+    a0 = np.array([0.25, 1.5], np.float32)
+    w1, a1 = oracle.rowwise_adagrad(G, goff, w0, a0, 0.1, 1e-6)
+    perm = np.array([2, 0, 1, 4, 3])
+    w2, a2 = oracle.rowwise_adagrad(G[perm], goff, w0[perm], a0, 0.1, 1e-6)
+    assert np.array_equal(a1, a2) and np.array_equal(w1[perm], w2)
+    assert a1[0] == np.float32(0.25) + np.float32(169.0 / 3) and a1[1] == np.float32(1.5) + np.float32(2.5)
+    # half weights: read exactly, rounded to nearest-even like numpy's cast
+    wh, _ = oracle.rowwise_adagrad(G, goff, w0.astype(np.float16), a0, 0.1, 1e-6)
+    assert np.array_equal(wh, w1.astype(np.float16))
+
+
 # ------------------------------------------------------------------ fmix64
 
 def _rotl(x, r):
