@@ -87,10 +87,16 @@ typedef enum {
 typedef enum { EMB_F32 = 0, EMB_F16 = 1, EMB_F16_MASTER = 2 } emb_dtype;
 
 /* The sparse optimizer a table is created for (JD ads article 3.2.1 names
- * Adagrad and FTRL).  Adagrad keeps one f32 accumulator per element; FTRL
- * keeps two f32 state values per element, n (in the accumulator array) and
- * z.  A backward call of the other optimizer is refused. */
-typedef enum { EMB_OPT_ADAGRAD = 0, EMB_OPT_FTRL = 1 } emb_optimizer;
+ * Adagrad and FTRL).  Adagrad keeps one f32 accumulator per element; row-wise
+ * Adagrad keeps one f32 accumulator per row (key) and adds the mean of the
+ * row's squared gradient to it (the pages give no formula for this variant;
+ * this is the reading); FTRL keeps two f32 state values per element, n (in
+ * the accumulator array) and z.  The Adagrad entry points apply the rule of
+ * the table (element-wise or row-wise); a backward call of the other
+ * optimizer family is refused.  Accumulator arrays (emb_table_create's acc,
+ * emb_table_export's acc_out, emb_table_export_rows' acc_out_d) hold one
+ * value per element, or per key for row-wise tables. */
+typedef enum { EMB_OPT_ADAGRAD = 0, EMB_OPT_FTRL = 1, EMB_OPT_ROWWISE_ADAGRAD = 2 } emb_optimizer;
 typedef enum { EMB_POOL_SUM = 0, EMB_POOL_MEAN = 1 } emb_pool;
 
 /* Device flag bits reported by emb_check_device_flag. */
@@ -119,7 +125,8 @@ typedef struct {
   emb_dtype wdtype;        /* weight storage type */
   int64_t capacity;        /* slots: power of two >= 2*n_keys; 0 = the smallest such */
   float acc_init;          /* accumulator (FTRL: n) value used when emb_table_create gets acc == NULL */
-  emb_optimizer optimizer; /* EMB_OPT_ADAGRAD (0) or EMB_OPT_FTRL; FTRL tables start with z = 0 */
+  emb_optimizer optimizer; /* EMB_OPT_ADAGRAD (0), EMB_OPT_FTRL (FTRL tables start with z = 0) or
+                              EMB_OPT_ROWWISE_ADAGRAD */
 } emb_table_desc;
 
 /* FTRL-Proximal hyperparameters (McMahan et al., KDD 2013): alpha > 0,
@@ -160,7 +167,8 @@ typedef struct {
  *            dim(slot(key_i)) elements of wdtype (float, IEEE half, or float
  *            for EMB_F16_MASTER: the master rows, whose f16 copy is made
  *            here).  NULL fills the weights with zeros.
- *   acc      host or device float32, same element layout as values; NULL fills
+ *   acc      host or device float32, same element layout as values (row-wise
+ *            tables: one value per key, in keys-array order); NULL fills
  *            with desc->acc_init.
  *   stream   stream for the uploads; the call synchronises it before return.
  *   out      receives the table handle (NULL on failure).
@@ -240,7 +248,10 @@ EMB_API emb_status emb_bwd_workspace_size(const emb_table* table, int64_t n_bags
  * to G[k]; the contributions of duplicate keys are reduced deterministically
  * (stable sort by row, fixed-order segmented sums); then for each hit key and
  * each element:  acc += g*g;  w -= lr*g / (sqrt(acc) + eps)  in float32
- * (half weights rounded to nearest-even).  Rows not hit are not touched.
+ * (half weights rounded to nearest-even).  On a row-wise table (one
+ * accumulator a per row of D elements):  a += (sum of g*g over the row) / D;
+ * then for each element  w -= lr*g / (sqrt(a) + eps).  Rows not hit are not
+ * touched.
  *   grad_out_d   float32[n_bags/n_slots, sum_dims], 16-byte aligned (read with
  *                16-byte vector loads; INVALID_ARG otherwise).
  *   workspace_d  device scratch of at least emb_bwd_workspace_size() bytes,
@@ -400,7 +411,8 @@ EMB_API emb_status emb_table_export(const emb_table* table, int64_t* keys_out, v
  * same passage (the rows a step updated, e.g. from emb_bwd_unique_keys): the
  * weights and accumulators of selected keys-array rows (ext_rows_d int64[n], indices into the keys array
  * given at creation).  Outputs are device buffers laid out [n, max_dim]: row
- * i's dim(slot) elements first, zero padding after.  Either output may be
+ * i's dim(slot) elements first, zero padding after (the accumulators of a
+ * row-wise table: [n], one per row).  Either output may be
  * NULL.  An index outside [0, n_keys) yields a zero row and raises
  * EMB_FLAG_BAD_ROW.  Enqueued on `stream`.
  */

@@ -40,7 +40,7 @@ EMB_SORT_DIGIT_BITS = 7
 BWD_PHASES = ("expand", "sort", "reduce", "fixup")
 _DTYPE = {"f32": 0, "f16": 1, "f16m": 2}   # f16m: f32 master rows + the f16 copy the forward reads
 _POOL = {"sum": 0, "mean": 1}
-_OPT = {"adagrad": 0, "ftrl": 1}
+_OPT = {"adagrad": 0, "ftrl": 1, "rowwise_adagrad": 2}
 
 
 class LibraryNotBuilt(ImportError):
@@ -227,7 +227,8 @@ def emb_table_create(dims, wdtype: str, keys: torch.Tensor, values: Optional[tor
                      acc: Optional[torch.Tensor] = None, capacity: int = 0, acc_init: float = 0.0,
                      stream=None, optimizer: str = "adagrad") -> Table:
     """keys: CPU int64; values/acc: CPU or CUDA, ragged rows in keys order.
-    optimizer: "adagrad" or "ftrl" (acc is then FTRL's n; z starts at 0)."""
+    optimizer: "adagrad", "ftrl" (acc is then FTRL's n; z starts at 0) or
+    "rowwise_adagrad" (acc holds one value per key, in keys order)."""
     if keys.is_cuda:
         raise ValueError("keys must be host memory (the table is prepared on the host)")
     wt = torch.float16 if wdtype == "f16" else torch.float32
@@ -428,13 +429,15 @@ def emb_table_export(table: Table, keys_out: Optional[torch.Tensor], values_out:
 
 def emb_table_export_rows(table: Table, rows: torch.Tensor, values_out: Optional[torch.Tensor] = None,
                           acc_out: Optional[torch.Tensor] = None, stream=None) -> Tuple[torch.Tensor, torch.Tensor]:
-    """Weights/accumulators of keys-array rows as [n, max_dim] device tensors (zero padded)."""
+    """Weights/accumulators of keys-array rows as [n, max_dim] device tensors (zero padded);
+    a row-wise Adagrad table's accumulators come as [n]."""
     n, md = rows.numel(), max(table.dims)
     wt = torch.float16 if table.wdtype == "f16" else torch.float32
     if values_out is None:
         values_out = torch.empty((n, md), dtype=wt, device=rows.device)
     if acc_out is None:
-        acc_out = torch.empty((n, md), dtype=torch.float32, device=rows.device)
+        shape = (n,) if table.optimizer == "rowwise_adagrad" else (n, md)
+        acc_out = torch.empty(shape, dtype=torch.float32, device=rows.device)
     _check(lib().emb_table_export_rows(table.handle, _cuda(rows, torch.int64, "rows"), n,
                                        _cuda(values_out, wt, "values_out"), _cuda(acc_out, torch.float32, "acc_out"),
                                        _stream(stream)))

@@ -685,7 +685,8 @@ __device__ __forceinline__ void stw4(__half* p, const float (&v)[4]) {
 // the update well inside the float32 tolerance at a fraction of the
 // instructions of the correctly rounded sequences.
 struct AdagradStep {
-  static constexpr bool kZ = false;  // no second state array
+  static constexpr bool kZ = false;        // no second state array
+  static constexpr bool kRowWise = false;  // one accumulator per element
   float lr, eps;
   __device__ __forceinline__ void elem(float& w, float& a, float& /*z*/, float g) const {
     a = fmaf(g, g, a);
@@ -706,6 +707,7 @@ struct AdagradStep {
 // the oracle's keeps that cancellation identical on both sides.
 struct FtrlStep {
   static constexpr bool kZ = true;
+  static constexpr bool kRowWise = false;
   float alpha, beta, l1, l2;
   __device__ __forceinline__ void elem(float& w, float& n, float& z, float g) const {
     const float n1 = __fadd_rn(n, __fmul_rn(g, g));
@@ -721,6 +723,17 @@ struct FtrlStep {
       w = -__fdiv_rn(num, den);
     }
   }
+};
+
+// Row-wise Adagrad: Adagrad with one accumulator per row (key) instead of
+// one per element.  The pages give no formula for this variant; the reading
+// here adds the mean of the row's squared gradient:  a += (sum_d g_d^2) / D;
+// then every element  w -= lr*g / (sqrt(a) + eps), with the same fast sqrt and
+// divide as AdagradStep.  The accumulator array holds one f32 per row.
+struct RowAdagradStep {
+  static constexpr bool kZ = false;
+  static constexpr bool kRowWise = true;
+  float lr, eps;
 };
 
 // The update of 4 consecutive elements from e: weights, accumulators (and z)
@@ -780,6 +793,44 @@ __device__ __forceinline__ void update_cols(const TableView& t, long long e, con
   for (int h = 0; h < VW; h += 4) update4<TW>(t, e + h, g + h, o);
 }
 
+// Row-wise Adagrad on one row whose gradient is spread over a group of G
+// lanes: lane li holds columns (cc*G + li)*4 + j, j < 4, in g[cc][j].  The
+// squared gradient is summed per lane (columns ascending) and then across
+// the group with a fixed xor tree (deterministic); every lane of the group
+// computes the new accumulator, lane 0 writes it, and each lane updates its
+// own weights (and, for master-copy tables, their f16 copy).
+template <typename TW, int G, int NCB>
+__device__ __forceinline__ void rowwise_update(const TableView& t, unsigned row, long long e0, int D, int li,
+                                               unsigned gmask, const float (&g)[NCB][4], const RowAdagradStep& o) {
+  float ss = 0.f;
+#pragma unroll
+  for (int cc = 0; cc < NCB; ++cc) {
+    const int col = (cc * G + li) * 4;
+    if (col < D)
+#pragma unroll
+      for (int j = 0; j < 4; ++j) ss = fmaf(g[cc][j], g[cc][j], ss);
+  }
+#pragma unroll
+  for (int off = 1; off < G; off <<= 1) ss += __shfl_xor_sync(gmask, ss, off, G);
+  const float a = t.ACC[row] + ss / (float)D;
+  __syncwarp(gmask);  // every lane has read the old accumulator
+  if (li == 0) t.ACC[row] = a;
+  const float den = (a > 0.f ? a * rsqrtf(a) : 0.f) + o.eps;
+  TW* W = static_cast<TW*>(t.W);
+#pragma unroll
+  for (int cc = 0; cc < NCB; ++cc) {
+    const int col = (cc * G + li) * 4;
+    if (col < D) {
+      float wv[4];
+      ldw4(W + e0 + col, wv);
+#pragma unroll
+      for (int j = 0; j < 4; ++j) wv[j] -= __fdividef(o.lr * g[cc][j], den);
+      stw4(W + e0 + col, wv);
+      if (std::is_same<TW, float>::value && t.W16) stw4(t.W16 + e0 + col, wv);
+    }
+  }
+}
+
 // Geometry of a row taken from the feature slot of a bag that holds it (the
 // expand step only pairs a row with bags of its own slot).  ok is false for a
 // row outside that slot's range, which only stale workspace data can produce.
@@ -811,12 +862,16 @@ __device__ __forceinline__ void prefetch_l2(const void* p) { asm volatile("prefe
 
 // The weight and accumulator bytes of a row, pulled towards L2 ahead of its
 // read-modify-write.
-template <typename TW>
-__device__ __forceinline__ void prefetch_row(const TableView& t, const RowGeo& g) {
+template <typename TW, bool kRowAcc>
+__device__ __forceinline__ void prefetch_row(const TableView& t, const RowGeo& g, unsigned row) {
   const char* w = reinterpret_cast<const char*>(static_cast<const TW*>(t.W) + g.e0);
-  const char* a = reinterpret_cast<const char*>(t.ACC + g.e0);
   for (int o = 0; o < g.D * (int)sizeof(TW); o += 128) prefetch_l2(w + o);
-  for (int o = 0; o < g.D * 4; o += 128) prefetch_l2(a + o);
+  if (kRowAcc) {
+    prefetch_l2(t.ACC + row);
+  } else {
+    const char* a = reinterpret_cast<const char*>(t.ACC + g.e0);
+    for (int o = 0; o < g.D * 4; o += 128) prefetch_l2(a + o);
+  }
 }
 
 // VW consecutive floats of grad_out: one 16-byte read-only load.
@@ -988,10 +1043,22 @@ __global__ void __launch_bounds__(kRedWarps * 32, 8) segreduce_update_kernel(
         const StageMeta sm = mt[f];
         if (sm.D == 0) continue;
         if (sm.flags == 3) {
+          if constexpr (Opt::kRowWise) {
+            static_assert(VW == 4, "row-wise update takes 4 columns per lane block");
+            float gr[NCB][4];
 #pragma unroll
-          for (int cc = 0; cc < NCB; ++cc) {
-            const int col = (cc * G + li) * VW;
-            if (col < sm.D) update_cols<TW, VW>(t, sm.e0 + col, &st[f][col], opt);
+            for (int cc = 0; cc < NCB; ++cc) {
+              const int col = (cc * G + li) * VW;
+#pragma unroll
+              for (int j = 0; j < 4; ++j) gr[cc][j] = col < sm.D ? st[f][col + j] : 0.f;
+            }
+            rowwise_update<TW, G, NCB>(t, sm.row, sm.e0, sm.D, li, gmask, gr, opt);
+          } else {
+#pragma unroll
+            for (int cc = 0; cc < NCB; ++cc) {
+              const int col = (cc * G + li) * VW;
+              if (col < sm.D) update_cols<TW, VW>(t, sm.e0 + col, &st[f][col], opt);
+            }
           }
         } else {
           float* dst = ((sm.flags & 1) ? partA : partB) + (size_t)c * maxd;
@@ -1065,7 +1132,7 @@ __global__ void __launch_bounds__(kRedWarps * 32, 8) segreduce_update_kernel(
       }
       if (use && start) {
         const RowGeo g = geo_from_slot(t, kk, sj);
-        if (g.ok) prefetch_row<TW>(t, g);
+        if (g.ok) prefetch_row<TW, Opt::kRowWise>(t, g, kk);
       }
       __syncwarp(gmask);
       // ---- in-order walk, U positions in flight per lane.  Positions past
@@ -1336,7 +1403,13 @@ __global__ void __launch_bounds__(256) fixup_kernel(TableView t, const unsigned*
         }
         acc[cc][j] = __fadd_rn(acc[cc][j], cmp[cc][j]);
       }
-    if (sub == 0) update_row<TW, NCB>(t, e0, D, G, li, acc, opt);
+    if constexpr (Opt::kRowWise) {
+      // after the xor tree every group holds the row's totals; group 0 applies the update
+      const unsigned gm = G == 32 ? 0xffffffffu : (((1u << G) - 1u) << (sub * G));
+      if (sub == 0) rowwise_update<TW, G, NCB>(t, row, e0, D, li, gm, acc, opt);
+    } else {
+      if (sub == 0) update_row<TW, NCB>(t, e0, D, G, li, acc, opt);
+    }
   }
 }
 
@@ -1593,12 +1666,19 @@ static emb_status sort_placed_pairs(const emb_table* table, int64_t n_bags, unsi
   return EMB_OK;
 }
 
-// The optimizer of one backward call.
+// The optimizer of one backward call.  The Adagrad entry points serve both
+// Adagrad tables (one accumulator per element) and row-wise Adagrad tables
+// (one per row); the table's optimizer picks the update.
 struct BwdOpt {
   bool ftrl;
   AdagradStep ada;
   FtrlStep fp;
 };
+
+static bool opt_fits_table(const emb_table* t, const BwdOpt& o) {
+  return o.ftrl ? t->optimizer == EMB_OPT_FTRL
+                : (t->optimizer == EMB_OPT_ADAGRAD || t->optimizer == EMB_OPT_ROWWISE_ADAGRAD);
+}
 
 // The backward.  With `recorded`, the (row, bag) pairs, 1/L and the header were
 // written by emb_lookup_fwd_record (or emb_lookup_fwd_dedup, which also sorted
@@ -1651,12 +1731,17 @@ static emb_status run_bwd(emb_table* table, const int64_t* offsets_d, int64_t n_
   const bool half = table->st.wdtype == EMB_F16;
   const unsigned nb = (unsigned)n_bags;
   cudaError_t e;
-  if (opt.ftrl)
+  if (opt.ftrl) {
     e = half ? dispatch_reduce<__half>(table, ki, vi, scale, mean, grad_out_d, n, nb, L, ws, opt.fp, st)
              : dispatch_reduce<float>(table, ki, vi, scale, mean, grad_out_d, n, nb, L, ws, opt.fp, st);
-  else
+  } else if (table->optimizer == EMB_OPT_ROWWISE_ADAGRAD) {
+    const RowAdagradStep ro{opt.ada.lr, opt.ada.eps};
+    e = half ? dispatch_reduce<__half>(table, ki, vi, scale, mean, grad_out_d, n, nb, L, ws, ro, st)
+             : dispatch_reduce<float>(table, ki, vi, scale, mean, grad_out_d, n, nb, L, ws, ro, st);
+  } else {
     e = half ? dispatch_reduce<__half>(table, ki, vi, scale, mean, grad_out_d, n, nb, L, ws, opt.ada, st)
              : dispatch_reduce<float>(table, ki, vi, scale, mean, grad_out_d, n, nb, L, ws, opt.ada, st);
+  }
   if (e != cudaSuccess) return cuda_fail(e, "segmented reduce launch");
   return EMB_OK;
 }
@@ -1813,7 +1898,8 @@ emb_status emb_bwd_adagrad_noalloc(emb_table* table, const int64_t* offsets_d, i
                                    void* stream) {
   emb_status rc = check_batch(table, offsets_d, n_bags, keys_d, nnz, pool);
   if (rc != EMB_OK) return rc;
-  if (table->optimizer != EMB_OPT_ADAGRAD) return fail(EMB_ERR_INVALID_ARG, "the table's optimizer is not Adagrad");
+  if (!opt_fits_table(table, BwdOpt{false, {lr, eps}, {}}))
+    return fail(EMB_ERR_INVALID_ARG, "the table's optimizer is not Adagrad");
   if (n_bags > 0 && !grad_out_d) return fail(EMB_ERR_INVALID_ARG, "grad_out is NULL");
   if (((uintptr_t)grad_out_d & 15) != 0) return fail(EMB_ERR_INVALID_ARG, "grad_out must be 16-byte aligned");
   const WsLayout L = ws_layout(table, n_bags, nnz);
@@ -1867,8 +1953,8 @@ emb_status emb_lookup_fwd_record(emb_table* table, const int64_t* offsets_d, int
 static emb_status bwd_recorded(emb_table* table, int64_t n_bags, int64_t nnz, emb_pool pool, const float* grad_out_d,
                                const BwdOpt& opt, void* workspace_d, size_t ws_bytes, void* stream) {
   if (!table) return fail(EMB_ERR_INVALID_ARG, "table is NULL");
-  if (table->optimizer != (opt.ftrl ? EMB_OPT_FTRL : EMB_OPT_ADAGRAD))
-    return fail(EMB_ERR_INVALID_ARG, "the table was created for the other optimizer");
+  if (!opt_fits_table(table, opt))
+    return fail(EMB_ERR_INVALID_ARG, "the table was created for another optimizer");
   if (!workspace_d || workspace_d != table->rec_ws || nnz != table->rec_nnz || n_bags != table->rec_bags ||
       (int)pool != table->rec_pool)
     return fail(EMB_ERR_INVALID_ARG, "no emb_lookup_fwd_record of this batch shape in this workspace");
@@ -1886,8 +1972,8 @@ static emb_status bwd_workspace(emb_table* table, const int64_t* offsets_d, int6
                                 void* workspace_d, size_t ws_bytes, void* stream) {
   emb_status rc = check_batch(table, offsets_d, n_bags, keys_d, nnz, pool);
   if (rc != EMB_OK) return rc;
-  if (table->optimizer != (opt.ftrl ? EMB_OPT_FTRL : EMB_OPT_ADAGRAD))
-    return fail(EMB_ERR_INVALID_ARG, "the table was created for the other optimizer");
+  if (!opt_fits_table(table, opt))
+    return fail(EMB_ERR_INVALID_ARG, "the table was created for another optimizer");
   if (n_bags > 0 && !grad_out_d) return fail(EMB_ERR_INVALID_ARG, "grad_out is NULL");
   if (((uintptr_t)grad_out_d & 15) != 0) return fail(EMB_ERR_INVALID_ARG, "grad_out must be 16-byte aligned");
   const WsLayout L = ws_layout(table, n_bags, nnz);

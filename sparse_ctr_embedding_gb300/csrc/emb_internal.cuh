@@ -8,7 +8,9 @@
 //   W       wdtype[n_elems]  weights, internal row order.  Rows of one feature
 //                            slot are contiguous (slot-major), so a row's
 //                            first element is elem_base[s] + (row - row_base[s]) * dim[s].
-//   ACC     f32[n_elems]     Adagrad accumulators, same layout as W.
+//   ACC     f32[n_elems]     Adagrad accumulators, same layout as W;
+//                            f32[n_rows] (one per internal row) for
+//                            EMB_OPT_ROWWISE_ADAGRAD tables.
 //   W16     f16[n_elems]     EMB_F16_MASTER tables only: the f16 copy of W
 //                            (then the f32 master) that the forward reads.
 //   Z       f32[n_elems]     EMB_OPT_FTRL tables only: FTRL's z (ACC is n).

@@ -95,7 +95,8 @@ emb_status check_desc(const emb_table_desc* d, int64_t n, int64_t* cap_out, int*
     return fail(EMB_ERR_INVALID_ARG, "n_slots must be in [1, 65535] with slot_dim given");
   if (d->wdtype != EMB_F32 && d->wdtype != EMB_F16 && d->wdtype != EMB_F16_MASTER)
     return fail(EMB_ERR_INVALID_ARG, "bad wdtype");
-  if (d->optimizer != EMB_OPT_ADAGRAD && d->optimizer != EMB_OPT_FTRL) return fail(EMB_ERR_INVALID_ARG, "bad optimizer");
+  if (d->optimizer != EMB_OPT_ADAGRAD && d->optimizer != EMB_OPT_FTRL && d->optimizer != EMB_OPT_ROWWISE_ADAGRAD)
+    return fail(EMB_ERR_INVALID_ARG, "bad optimizer");
   const int vec = d->wdtype == EMB_F32 ? 4 : 8;
   int max_dim = 0;
   long long sum_dims = 0;
@@ -301,7 +302,8 @@ __global__ void slots_kernel(const Slot* slots, long long p0, long long p1, long
 // Selected keys-array rows to a dense [n, max_dim] buffer (zero padded).
 template <typename T>
 __global__ void export_rows_kernel(TableView t, const unsigned* ext_to_int, const long long* __restrict__ rows,
-                                   long long n, unsigned n_keys, T* __restrict__ vout, float* __restrict__ aout) {
+                                   long long n, unsigned n_keys, T* __restrict__ vout, float* __restrict__ aout,
+                                   int acc_per_row) {
   const int lane = threadIdx.x & 31;
   const T* W = static_cast<const T*>(t.W);
   long long i = (blockIdx.x * (long long)blockDim.x + threadIdx.x) >> 5;
@@ -312,8 +314,9 @@ __global__ void export_rows_kernel(TableView t, const unsigned* ext_to_int, cons
     if (!ok && lane == 0) atomicOr(t.flags, EMB_FLAG_BAD_ROW);
     int D = 0;
     long long ie = 0;
+    unsigned r = 0;
     if (ok) {
-      const unsigned r = ext_to_int[e];
+      r = ext_to_int[e];
       const SlotInfo si = t.sinfo[key_slot(t.row_key[r])];
       D = si.dim;
       ie = row_elem(si, r);
@@ -321,8 +324,9 @@ __global__ void export_rows_kernel(TableView t, const unsigned* ext_to_int, cons
     for (int j = lane; j < t.max_dim; j += 32) {
       const bool in = j < D;
       if (vout) vout[i * t.max_dim + j] = in ? W[ie + j] : T(0);
-      if (aout) aout[i * t.max_dim + j] = in ? t.ACC[ie + j] : 0.f;
+      if (aout && !acc_per_row) aout[i * t.max_dim + j] = in ? t.ACC[ie + j] : 0.f;
     }
+    if (aout && acc_per_row && lane == 0) aout[i] = ok ? t.ACC[r] : 0.f;
   }
 }
 
@@ -357,6 +361,47 @@ static bool is_device_ptr(const void* p) {
 
 static long long ext_elem_h(const emb_table* t, const std::vector<long long>& off, unsigned e) {
   return off.empty() ? (long long)e * t->uniform_dim : off[e];
+}
+
+// One f32 per key between keys-array order (src or dst) and internal row order.
+template <bool kToTable>
+__global__ void permute_keys_kernel(const unsigned* __restrict__ ext_to_int, unsigned n, const float* __restrict__ src,
+                                    float* __restrict__ dst) {
+  for (unsigned e = blockIdx.x * blockDim.x + threadIdx.x; e < n; e += gridDim.x * blockDim.x) {
+    if (kToTable) dst[ext_to_int[e]] = src[e];
+    else dst[e] = src[ext_to_int[e]];
+  }
+}
+
+// Move one f32 per key (row-wise accumulators) between a caller buffer in
+// keys-array order (host or device) and the table's array in internal order.
+static emb_status move_keyvals(const emb_table* t, const float* user, float* table_arr, bool to_table,
+                               cudaStream_t st) {
+  const unsigned n = (unsigned)t->st.n_keys;
+  if (n == 0) return EMB_OK;
+  const bool dev = is_device_ptr(user);
+  float* buf = (float*)user;
+  if (!dev) {
+    EMB_CUDA(dmalloc((void**)&buf, (size_t)n * 4));
+    if (to_table) {
+      cudaError_t ce = cudaMemcpyAsync(buf, user, (size_t)n * 4, cudaMemcpyHostToDevice, st);
+      if (ce != cudaSuccess) {
+        dfree(buf);
+        return cuda_fail(ce, "cudaMemcpyAsync(accumulators to device)");
+      }
+    }
+  }
+  if (to_table)
+    permute_keys_kernel<true><<<grid_for(n, 256), 256, 0, st>>>(t->ext_to_int_d, n, buf, table_arr);
+  else
+    permute_keys_kernel<false><<<grid_for(n, 256), 256, 0, st>>>(t->ext_to_int_d, n, table_arr, buf);
+  cudaError_t ce = cudaGetLastError();
+  if (ce == cudaSuccess && !dev && !to_table)
+    ce = cudaMemcpyAsync((void*)user, buf, (size_t)n * 4, cudaMemcpyDeviceToHost, st);
+  if (ce == cudaSuccess && !dev) ce = cudaStreamSynchronize(st);
+  if (!dev) dfree(buf);
+  if (ce != cudaSuccess) return cuda_fail(ce, "moving per-key accumulators");
+  return EMB_OK;
 }
 
 // Move ragged rows between a caller buffer in keys-array order (host or
@@ -469,8 +514,10 @@ emb_status finish_table(emb_table* t, const emb_table_desc* desc, const void* va
   const size_t ne = (size_t)std::max<long long>(t->st.n_elems, 1);
   EMB_CUDA(dmalloc(&t->W_d, ne * esz));
   bytes += ne * esz;
-  EMB_CUDA(dmalloc((void**)&t->ACC_d, ne * 4));
-  bytes += ne * 4;
+  const bool rowwise = desc->optimizer == EMB_OPT_ROWWISE_ADAGRAD;
+  const size_t na = rowwise ? (size_t)std::max<long long>(t->st.n_keys, 1) : ne;  // accumulators
+  EMB_CUDA(dmalloc((void**)&t->ACC_d, na * 4));
+  bytes += na * 4;
   t->st.device_bytes = bytes;
   if (values) {
     if ((r = move_rows(t, values, t->W_d, esz, true, st)) != EMB_OK) return r;
@@ -486,9 +533,10 @@ emb_status finish_table(emb_table* t, const emb_table_desc* desc, const void* va
     EMB_CUDA(cudaGetLastError());
   }
   if (acc) {
-    if ((r = move_rows(t, acc, t->ACC_d, 4, true, st)) != EMB_OK) return r;
+    if ((r = rowwise ? move_keyvals(t, acc, t->ACC_d, true, st) : move_rows(t, acc, t->ACC_d, 4, true, st)) != EMB_OK)
+      return r;
   } else {
-    fill_f32_kernel<<<grid_for((long long)ne, 256), 256, 0, st>>>(t->ACC_d, (long long)ne, desc->acc_init);
+    fill_f32_kernel<<<grid_for((long long)na, 256), 256, 0, st>>>(t->ACC_d, (long long)na, desc->acc_init);
     EMB_CUDA(cudaGetLastError());
   }
   if (desc->optimizer == EMB_OPT_FTRL) {  // FTRL's z starts at zero (emb_table_import_z sets it)
@@ -613,7 +661,11 @@ emb_status emb_table_export(const emb_table* table, int64_t* keys_out, void* val
   const size_t esz = table->st.wdtype == EMB_F16 ? 2 : 4;
   emb_status r;
   if (values_out && (r = move_rows(table, values_out, table->W_d, esz, false, st)) != EMB_OK) return r;
-  if (acc_out && (r = move_rows(table, acc_out, table->ACC_d, 4, false, st)) != EMB_OK) return r;
+  if (acc_out) {
+    r = table->optimizer == EMB_OPT_ROWWISE_ADAGRAD ? move_keyvals(table, acc_out, table->ACC_d, false, st)
+                                                    : move_rows(table, acc_out, table->ACC_d, 4, false, st);
+    if (r != EMB_OK) return r;
+  }
   if (keys_out && n) {
     if (is_device_ptr(keys_out)) {
       export_keys_kernel<<<grid_for(n, 256), 256, 0, st>>>(table->row_key_d, table->ext_to_int_d, 0, n,
@@ -661,14 +713,15 @@ emb_status emb_table_export_rows(const emb_table* table, const int64_t* ext_rows
   cudaStream_t st = (cudaStream_t)stream;
   const int grid = grid_for(n * 32, 256);
   const unsigned nk = (unsigned)table->st.n_keys;
+  const int rw = table->optimizer == EMB_OPT_ROWWISE_ADAGRAD ? 1 : 0;
   if (table->st.wdtype == EMB_F16)
     export_rows_kernel<unsigned short><<<grid, 256, 0, st>>>(table->view(), table->ext_to_int_d,
                                                              (const long long*)ext_rows_d, n, nk,
-                                                             (unsigned short*)values_out_d, acc_out_d);
+                                                             (unsigned short*)values_out_d, acc_out_d, rw);
   else
     export_rows_kernel<unsigned><<<grid, 256, 0, st>>>(table->view(), table->ext_to_int_d,
                                                        (const long long*)ext_rows_d, n, nk, (unsigned*)values_out_d,
-                                                       acc_out_d);
+                                                       acc_out_d, rw);
   EMB_CUDA(cudaGetLastError());
   return EMB_OK;
 }
