@@ -265,10 +265,10 @@ def emb_table_get_stats(table: Table) -> dict:
     return s.as_dict()
 
 
-def emb_table_plan(dims, wdtype: str, keys, capacity: int = 0, layout: bool = False):
+def emb_table_plan(dims, wdtype: str, keys, capacity: int = 0, layout: bool = False, optimizer: str = "adagrad"):
     """Host-only validation/statistics; with layout=True also the slot layout (numpy)."""
     keys = np.ascontiguousarray(keys, dtype=np.int64)
-    d, _keep = _desc(dims, wdtype, capacity, 0.0)
+    d, _keep = _desc(dims, wdtype, capacity, 0.0, optimizer)
     s = _Stats()
     sk = sr = None
     if layout:

@@ -101,6 +101,20 @@ def test_master_copy_tables_plan_like_f16_tables():
 
 
 
+def test_plan_accepts_each_optimizer_and_rejects_an_unknown_one():
+    keys = (np.arange(20, dtype=np.int64) * 7919) | (1 << 48)
+    base, sk0, _ = E.emb_table_plan([8, 8], "f32", keys, 64, layout=True)
+    for opt in ("ftrl", "rowwise_adagrad"):          # the optimizer changes no part of the layout
+        st, sk, _ = E.emb_table_plan([8, 8], "f32", keys, 64, layout=True, optimizer=opt)
+        assert np.array_equal(sk, sk0) and st["n_elems"] == base["n_elems"]
+    d, _keep = E._desc([8, 8], "f32", 64, 0.0)
+    d.optimizer = 3
+    s = E._Stats()
+    with pytest.raises(E.EmbError) as ei:
+        E._check(E.lib().emb_table_plan(ctypes.byref(d), keys.ctypes.data, keys.size, ctypes.byref(s), None, None))
+    assert ei.value.name == "EMB_ERR_INVALID_ARG"
+
+
 def test_failed_create_returns_oom_and_leaves_nothing_allocated():
     """Fault injection on the host: the table's first device allocation fails;
     create must return EMB_ERR_OOM (not abort) and hold no device memory.
