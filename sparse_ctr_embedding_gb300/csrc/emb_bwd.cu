@@ -1116,9 +1116,10 @@ __global__ void __launch_bounds__(kRedWarps * 32, 8) segreduce_update_kernel(
       const bool start = valid && (kk != kp || (i0 == cs && li == 0));
       // Only positions that add something or start a row are walked: merged
       // duplicates, and misses after the first position of their run, are
-      // dropped (about 30% of the positions of a Zipf batch).  The kept ones
-      // take consecutive walk indices in window order; smask marks the walk
-      // indices of row starts.  The window's first position is always kept.
+      // dropped (30% of the positions with Zipf bag lengths up to 256).  The
+      // kept ones take consecutive walk indices in window order; smask marks
+      // the walk indices of row starts.  The sub-chunk's first position is a
+      // start, so it is walk index 0 of the sub-chunk's first window.
       const bool keep = use || start;
       const unsigned kmask = (__ballot_sync(gmask, keep) >> (sub * G)) & gbits;
       const int nk = __popc(kmask);
