@@ -50,6 +50,27 @@ def test_recorded_step_parity_and_identity(cfg):
     assert np.array_equal(np.sort(rec.unique), np.sort(ref.unique))
 
 
+# The 100M-key workload's structure (Zipf bag lengths up to 256, so many
+# repeated keys within a bag; 5% absent keys; mean pooling) with rows of 4 and
+# 8 elements: one and two lanes per row in the reduce, whose windows then hold
+# one and two positions.
+NARROW = [
+    W.scaled(W.config(5), 1000, 256, name="64slot-4d-f32-mean", dims=(4,) * 64, wdtype="f32"),
+    W.scaled(W.config(5), 1000, 256, name="64slot-8d-f16-mean", dims=(8,) * 64),
+]
+
+
+@pytest.mark.parametrize("cfg", NARROW, ids=lambda c: c.name)
+def test_narrow_rows_parity_both_paths(cfg):
+    wl = W.make(cfg, device="cuda")
+    rec = gpu_step(cfg, wl, recorded=True)
+    report(f"narrow/{cfg.name}/recorded", **check_step(cfg, wl, rec))
+    ref = gpu_step(cfg, wl)
+    assert torch.equal(rec.out, ref.out)
+    assert np.array_equal(rec.values_out.view(np.uint8), ref.values_out.view(np.uint8))
+    assert np.array_equal(rec.acc_out.view(np.uint8), ref.acc_out.view(np.uint8))
+
+
 def test_recorded_backward_needs_its_forward():
     cfg = SMALL[0]
     wl = W.make(cfg, device="cuda")
